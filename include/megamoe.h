@@ -1,0 +1,226 @@
+/*
+ * megamoe.h -- C ABI of the GB300 (sm_103a) fused MoE expert layer.
+ *
+ * One call runs the whole single-GPU hot path of the fused "MegaMoE" expert
+ * layer: route the (token, k) assignments to experts, L1 gate/up grouped GEMM
+ * (FP8-E4M3 activations x FP4-E2M1 weights, one UE8M0 scale per 32 elements
+ * along K), clamp + SwiGLU + FP8 requantisation, L2 down grouped GEMM, and the
+ * top-k weighted combine into a bf16 output.
+ *
+ * Sources (the pages this library follows):
+ *  [P1] sglang PR #36657 "[Blackwell] Reserve SMs for DeepGEMM MegaMoE grid
+ *       barriers" -- Summary, Root cause, Fix: an even clustered grid with a
+ *       whole-grid software barrier; the launch size is the physical SM count
+ *       minus a reserve (default 2), floored at 2 and rounded down to even.
+ *  [P2] the prhub.com.cn digest of the same PR -- 实现拆解 and 关键源码片段:
+ *       the env default of 2 reserved SMs, the reserve arithmetic, the call
+ *       fp8_fp4_mega_moe(y, l1_weights, l2_weights, buf, recipe=(1, 1, 32),
+ *       activation="swiglu", activation_clamp=swiglu_limit, fast_math=True),
+ *       and a symmetric-buffer cache keyed only on the shape.
+ *  [P3] DeepGEMM "SM90 MegaMoE 开发日志" -- Phase 1 entry (the buffer views
+ *       x, x_sf, topk_idx, topk_weights, l1_acts, l1_acts_sf, l2_acts,
+ *       l2_acts_sf; a workspace-size query) and Phase 2 entry (dispatch:
+ *       workspace clean, expert count, source token-topk index write,
+ *       token source metadata, l1_arrival_count release).
+ *  [P4] DeepGEMM PR #451 "[Bugfix] Reset MegaMoE combine readiness for CUDA
+ *       graph replay": readiness flags are reset by every launch, never keyed
+ *       on %gridid, so graph replays match eager runs exactly.
+ *
+ * Conventions for every entry point:
+ *  - All tensors are row-major and live in device memory unless a comment says
+ *    "host".  The caller owns every buffer; the library allocates no device
+ *    memory and keeps no per-call state.
+ *  - Calls are stream-ordered on `stream` (a cudaStream_t; 0 = legacy default
+ *    stream).  Argument errors are returned synchronously before anything is
+ *    enqueued.  Errors found on the device (a bad expert index, a wait that
+ *    timed out) are written to the status word at the head of the workspace
+ *    and read back with mm_get_status().
+ *  - Return values are mm_status codes (0 = success, negative = error) unless
+ *    stated otherwise.
+ */
+#ifndef MEGAMOE_H
+#define MEGAMOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream handle (binary-compatible with cudaStream_t / CUstream). */
+typedef struct CUstream_st* mm_stream_t;
+
+typedef enum {
+  MM_OK = 0,
+  MM_ERR_INVALID_ARG = -1,         /* null pointer, misaligned pointer, bad value     */
+  MM_ERR_UNSUPPORTED_SHAPE = -2,   /* dimensions outside the supported envelope       */
+  MM_ERR_WORKSPACE_TOO_SMALL = -3, /* workspace_bytes < mm_workspace_size(...)        */
+  MM_ERR_CUDA = -4,                /* a CUDA runtime/driver call failed               */
+  MM_ERR_TIMEOUT = -5,             /* a device wait (grid barrier, readiness counter,
+                                      pipeline barrier) ran past its time limit       */
+  MM_ERR_BAD_INDEX = -6,           /* topk_idx outside [-1, experts)                  */
+  MM_ERR_BOUNDS = -7,              /* reserved for checked builds                     */
+  MM_ERR_NO_DEVICE = -8            /* no usable sm_103 device                         */
+} mm_status;
+
+/* Element formats accepted by mm_quantize_mx. */
+typedef enum { MM_FMT_E4M3 = 0, MM_FMT_E2M1 = 1 } mm_format;
+
+/*
+ * Supported shapes (checked by every entry point that takes dimensions):
+ *   hidden  H : multiple of 128, 128 <= H <= 32768
+ *   inter   I : multiple of 128, 128 <= I <= 16384  (the packed-FP4 TMA tile
+ *               needs rows of a multiple of 128 elements)
+ *   experts E : 1 <= E <= 1024
+ *   topk    k : 1 <= k <= 16
+ *   tokens  T : 0 <= T, T * k <= 2^24
+ */
+
+/*
+ * mm_workspace_size -- bytes of device workspace that mm_forward / mm_route
+ * need for up to `max_tokens` tokens.  Depends only on the shape, never on the
+ * SM count or the reserve (the cache key of [P2] 实现拆解 item 5 holds only
+ * shape parameters).  Returns 0 for unsupported arguments.
+ * Workspace contents: a control block (status, abort flag, grid-barrier and
+ * readiness counters), routing results (counts, offsets, permutation), the
+ * dispatched tokens and their scales in expert order, the L1 activations
+ * (E4M3 + UE8M0/32) and the weighted L2 outputs (fp32) -- the views of [P3].
+ */
+size_t mm_workspace_size(int max_tokens, int experts, int topk, int hidden, int inter);
+
+/*
+ * mm_forward -- the fused layer, y = MoE(x).  ([P2] 关键源码片段, [P3])
+ *
+ *   num_tokens T, experts E, topk k, hidden H, inter I : the shape
+ *   x         E4M3 codes            [T, H]        16-byte aligned
+ *   x_sf      UE8M0 bytes           [T, H/32]     4-byte aligned
+ *   topk_idx  int32                 [T, k]        expert id, or -1 = empty slot
+ *   topk_w    float32               [T, k]        combine weight of each slot
+ *   l1_w      E2M1, two per byte    [E, 2I, H/2]  element 2c in the low nibble;
+ *             rows [0, I) are the gate projection, rows [I, 2I) the up
+ *             projection; 32-byte aligned
+ *   l1_sf     UE8M0 bytes           [E, 2I, H/32] 4-byte aligned
+ *   l2_w      E2M1, two per byte    [E, H, I/2]   32-byte aligned
+ *   l2_sf     UE8M0 bytes           [E, H, I/32]  4-byte aligned
+ *   y         bfloat16              [T, H]        16-byte aligned; fully written
+ *             (a token whose slots are all empty gets a zero row)
+ *   clamp     swiglu limit L: applies iff finite and > 0; then
+ *             gate = min(gate, L), up = min(max(up, -L), L) before SwiGLU
+ *   num_sms   SMs this launch may use; <= 0 means all.  The persistent grid is
+ *             min(num_sms, SMs - reserve) rounded down to even, at least 2
+ *             ([P1] Fix; [P2] 实现拆解 items 2-3), and never more CTAs than
+ *             can be resident at once.
+ *   workspace device buffer of at least mm_workspace_size(T', E, k, H, I)
+ *             bytes for some T' >= T, 256-byte aligned, owned by the caller;
+ *             one workspace must not be used by two launches that overlap.
+ *   stream    the stream to enqueue on.
+ *
+ * Enqueues two kernels (routing, then the persistent layer kernel) and
+ * returns.  T = 0 returns MM_OK without launching.  Device-side errors land in
+ * the workspace status (mm_get_status); the next mm_forward resets it.  Every
+ * device wait is bounded by mm_set_wait_timeout_ns; a wait that runs out sets
+ * MM_ERR_TIMEOUT and the kernel returns instead of hanging.  The call makes
+ * no host synchronisation and no allocation, so it can be captured in a CUDA
+ * graph; all counters and flags are reset by each launch ([P4]).
+ */
+int mm_forward(int num_tokens, int experts, int topk, int hidden, int inter,
+               const void* x, const void* x_sf, const int32_t* topk_idx, const float* topk_w,
+               const void* l1_w, const void* l1_sf, const void* l2_w, const void* l2_sf,
+               void* y, float clamp, int num_sms,
+               void* workspace, size_t workspace_bytes, mm_stream_t stream);
+
+/*
+ * mm_set_reserved_sms -- SMs left free for other streams by every launch
+ * ([P1] Summary: two by default; [P2] 实现拆解 item 1: 0 disables it).
+ * n < 0 is taken as 0.  Process-wide; read at each launch.  Returns the
+ * previous value.  The environment variable MM_RESERVED_SMS, if set when the
+ * library loads, replaces the default of 2.
+ */
+int mm_set_reserved_sms(int n);
+int mm_get_reserved_sms(void);
+
+/*
+ * mm_grid_size -- the launch-size rule, exposed for tests and callers:
+ *   cap    = max(2, device_sms - max(reserved_sms, 0))
+ *   want   = num_sms > 0 ? min(num_sms, device_sms) : device_sms
+ *   g      = min(cap, want);  g -= g % 2;  g = max(g, 2)
+ *   g      = min(g, max_resident) rounded down to even (if max_resident > 0)
+ * ([P2] 关键源码片段: _mega_moe_max_num_sms and the context manager).
+ * Returns the grid size, or MM_ERR_INVALID_ARG if device_sms < 2.  Host only.
+ */
+int mm_grid_size(int device_sms, int reserved_sms, int num_sms, int max_resident);
+
+/*
+ * mm_set_wait_timeout_ns -- time limit of every device-side wait (default
+ * 2e9 ns).  The pages' kernel reports "grid sync timeout: sm=.., thread=..,
+ * grid_sync_idx=.." instead of hanging ([P2] 功能与动机); here the wait
+ * records MM_ERR_TIMEOUT with the SM and the wait site, raises the abort flag
+ * and returns.  ns == 0 restores the default.  Process-wide.
+ */
+void mm_set_wait_timeout_ns(unsigned long long ns);
+unsigned long long mm_get_wait_timeout_ns(void);
+
+/*
+ * mm_get_status -- synchronises `stream`, then reads the status word of
+ * `workspace`.  *sm (may be NULL) receives the SM id that recorded the error;
+ * *info (may be NULL) the wait site ((site << 24) | tile) or the first bad
+ * flat index for MM_ERR_BAD_INDEX.  Returns the recorded mm_status (MM_OK if
+ * none) or MM_ERR_CUDA if the synchronisation or copy failed.
+ */
+int mm_get_status(const void* workspace, mm_stream_t stream, int* sm, int* info);
+
+/*
+ * mm_route -- runs only the routing kernel of mm_forward (reset, expert
+ * histogram, prefix scan, stable permutation) into `workspace` ([P3] Phase 2
+ * entry: expert count, source token-topk index write).  Same argument rules
+ * as mm_forward.  Test hook.
+ */
+int mm_route(int num_tokens, int experts, int topk, int hidden, int inter,
+             const int32_t* topk_idx, void* workspace, size_t workspace_bytes,
+             mm_stream_t stream);
+
+/*
+ * mm_read_routing -- synchronous copy of the routing results left in
+ * `workspace` by mm_route / mm_forward for the given shape into HOST buffers
+ * (any may be NULL): counts [E], offsets [E+1] (exclusive prefix of counts),
+ * perm [T*k] (slot -> flat index t*k+j; entries past offsets[E] are unused),
+ * inv [T*k] (flat index -> slot, -1 for an empty slot).  Synchronises the
+ * device.  Test hook.
+ */
+int mm_read_routing(int num_tokens, int experts, int topk, int hidden, int inter,
+                    const void* workspace, int32_t* counts, int32_t* offsets,
+                    int32_t* perm, int32_t* inv);
+
+/*
+ * mm_workspace_region -- byte offset and size of a named region of the
+ * workspace for the given shape, so tests can inspect intermediates:
+ *   0 control block   1 counts      2 offsets     3 work items  4 arrivals
+ *   5 L1-done counts  6 perm        7 inv         8 dispatched x [T*k, H]
+ *   9 dispatched x_sf [T*k, H/32]  10 l1_acts [T*k, I] (E4M3, slot order)
+ *  11 l1_acts_sf [T*k, I/32]        12 weighted L2 outputs, fp32 [T*k, H]
+ *     indexed by the flat assignment t*k+j
+ * Returns MM_OK, or MM_ERR_INVALID_ARG for an unknown region or shape.
+ */
+int mm_workspace_region(int which, int num_tokens, int experts, int topk, int hidden,
+                        int inter, size_t* offset, size_t* bytes);
+
+/*
+ * mm_quantize_mx -- block quantiser: src float32 [rows, cols] (cols a
+ * multiple of 32, 16-byte aligned) -> element codes and one UE8M0 scale per
+ * 32 consecutive elements of a row.  For each block with largest magnitude a,
+ * the scale exponent is the smallest s with a <= F * 2^s (F = 448 for E4M3,
+ * 6 for E2M1), clamped to [-127, 127], and 0 for an all-zero block; elements
+ * are round-to-nearest-even of v / 2^s.  dst: E4M3 -> [rows, cols] bytes;
+ * E2M1 -> [rows, cols/2] bytes, element 2c in the low nibble (16-byte
+ * aligned).  dst_sf: [rows, cols/32] bytes.  This is the quantisation that
+ * precedes the fused call ([P1] Fix: "pre-dispatch"; [P2] 关键源码片段) and
+ * the rule the layer applies to its L1 activations.
+ */
+int mm_quantize_mx(const float* src, long long rows, long long cols, int fmt,
+                   void* dst, void* dst_sf, mm_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MEGAMOE_H */

@@ -1,0 +1,335 @@
+// Shared definitions of the GB300 fused MoE expert layer: workspace layout,
+// tile geometry and thin inline-PTX wrappers (mbarrier, TMA, tcgen05).
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/megamoe.h"
+
+namespace mm {
+
+// ----------------------------------------------------------------- geometry
+constexpr int kBlockK = 128;        // K per pipeline stage: 4 UE8M0 scale blocks of 32
+constexpr int kL1Feat = 64;         // intermediate features per L1 tile (64 gate + 64 up rows)
+constexpr int kL2Rows = 128;        // hidden rows per L2 tile
+constexpr int kTileM = 128;         // MMA M (weight rows)
+constexpr int kMaxTileN = 240;      // tokens per tile (MMA N), multiple of 16
+constexpr int kStages = 4;          // smem pipeline depth
+constexpr int kThreads = 256;       // 8 warps per CTA
+
+constexpr int kABytes = kTileM * kBlockK;           // 16 KB: 128 rows x 128 padded FP4 bytes
+// A packed-FP4 TMA box counts its global (packed) bytes toward the barrier's
+// transaction count, not its padded shared-memory footprint.
+constexpr int kATxBytes = kTileM * kBlockK / 2;     // 8 KB per stage
+constexpr int kBBytes = kMaxTileN * kBlockK;        // 30 KB: 240 token rows x 128 B
+constexpr int kSFABytes = 512;                      // one 128-row scale atom
+constexpr int kSFBBytes = 1024;                     // two 128-row scale atoms
+constexpr int kStageBytes = kABytes + kBBytes + kSFABytes + kSFBBytes;
+static_assert(kABytes % 1024 == 0 && kBBytes % 1024 == 0, "SW128 tiles need 1 KB alignment");
+
+// TMEM columns: two accumulator buffers and the scale factors of one stage.
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAccStride = 256;                // buffer b starts at column 256*b
+constexpr uint32_t kSFACol = 496;                   // 4 columns
+constexpr uint32_t kSFBCol = 500;                   // 8 columns
+
+// Epilogue exchange buffer (two warp pairs x two directions x 8 columns x 32 lanes).
+constexpr int kXchgBytes = 2 * 2 * 8 * 32 * 4;
+
+constexpr int kSmemBytes = kStages * kStageBytes + 256 /*barriers*/ + kXchgBytes + 1024 /*align*/;
+
+// ----------------------------------------------------------------- control block
+// 32-bit words at the head of the workspace.
+enum CtrlWord : int {
+  kStatus = 0, kErrSm = 1, kErrInfo = 2, kAbort = 3, kGridBar = 4, kSiteMask = 5, kCtrlWords = 64
+};
+
+// Wait sites recorded in the error info word (site << 24 | tile & 0xFFFFFF).
+enum WaitSite : uint32_t {
+  kSiteFull = 1, kSiteEmpty = 2, kSiteTmemFull = 3, kSiteTmemEmpty = 4,
+  kSiteArrival = 5, kSiteL1Done = 6, kSiteGridBar = 7, kSiteDrain = 8, kSiteFullSf = 9
+};
+
+// ----------------------------------------------------------------- workspace
+struct Layout {
+  size_t ctrl, counts, offsets, items, arrival, l1_done, perm, inv;
+  size_t xs, xs_sf, l1a, l1a_sf, stage, total;
+};
+
+__host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+__host__ __device__ inline Layout make_layout(long long T, int E, int k, int H, int I) {
+  Layout L;
+  const size_t A = (size_t)T * (size_t)k;
+  size_t o = 0;
+  L.ctrl = o;     o = align256(o + 4 * kCtrlWords);
+  L.counts = o;   o = align256(o + 4 * (size_t)E);
+  L.offsets = o;  o = align256(o + 4 * (size_t)(E + 1));
+  L.items = o;    o = align256(o + 4 * (size_t)(E + 1));
+  L.arrival = o;  o = align256(o + 4 * (size_t)E);
+  L.l1_done = o;  o = align256(o + 4 * (size_t)E);
+  L.perm = o;     o = align256(o + 4 * A);
+  L.inv = o;      o = align256(o + 4 * A);
+  L.xs = o;       o = align256(o + A * (size_t)H);
+  L.xs_sf = o;    o = align256(o + A * (size_t)(H / 32));
+  L.l1a = o;      o = align256(o + A * (size_t)I);
+  L.l1a_sf = o;   o = align256(o + A * (size_t)(I / 32));
+  L.stage = o;    o = align256(o + A * (size_t)H * 4);
+  L.total = o;
+  return L;
+}
+
+// Number of tiles (MMA N blocks) an expert with `count` assignments splits into,
+// and the rows of block `b`: blocks are balanced, each at most kMaxTileN rows.
+__host__ __device__ inline int n_blocks(int count) { return (count + kMaxTileN - 1) / kMaxTileN; }
+
+// ----------------------------------------------------------------- parameters
+struct ForwardParams {
+  int T, E, k, H, I;
+  int A;                       // T * k
+  int mt1, mt2;                // L1 / L2 tiles per (expert, N block): I/64, H/128
+  int ks1, ks2;                // K stages of L1 / L2: H/128, I/128
+  int use_clamp;
+  float clamp;
+  unsigned long long timeout_ns;
+  const uint8_t* x;
+  const uint8_t* x_sf;
+  const int32_t* topk_idx;
+  const float* topk_w;
+  const uint8_t* w1_sf;
+  const uint8_t* w2_sf;
+  uint16_t* y;                 // bf16 bits
+  uint8_t* ws;
+  Layout L;
+};
+
+struct RouteParams {
+  int T, E, k;
+  int A;
+  const int32_t* topk_idx;
+  uint8_t* ws;
+  Layout L;
+};
+
+// ----------------------------------------------------------------- device helpers
+#if defined(__CUDACC__)
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint32_t smid() {
+  uint32_t s;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(s));
+  return s;
+}
+
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void red_release_add(uint32_t* p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_volatile(const uint32_t* p) {
+  return *reinterpret_cast<const volatile uint32_t*>(p);
+}
+
+// Generic-proxy global writes <-> async-proxy (TMA) global reads.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Record the first device-side error of a launch and raise the abort flag.
+__device__ __forceinline__ void set_error(uint32_t* ctrl, int code, uint32_t info) {
+  atomicOr(&ctrl[kSiteMask], 1u << ((info >> 24) & 31u));   // every wait site that gave up
+  if (atomicCAS(&ctrl[kStatus], 0u, (uint32_t)code) == 0u) {
+    ctrl[kErrSm] = smid();
+    ctrl[kErrInfo] = info;
+  }
+  __threadfence();
+  atomicExch(&ctrl[kAbort], 1u);
+}
+
+// ---- mbarrier
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(bar), "r"(bytes) : "memory");
+}
+
+// Bounded wait on an mbarrier phase: polls the abort flag and the global timer.
+// Returns false if the time limit passed or another thread raised the abort flag.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t* ctrl,
+                                          unsigned long long timeout_ns, uint32_t site) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  uint32_t it = 0;
+  while (!mbar_try_wait(bar, parity)) {
+    if ((++it & 63u) == 0u) {
+      if (ld_volatile(&ctrl[kAbort]) != 0u) return false;
+      if (globaltimer() - t0 > timeout_ns) {
+        set_error(ctrl, MM_ERR_TIMEOUT, site);
+        return false;
+      }
+    }
+  }
+  return true;
+}
+
+// Bounded wait until a global counter reaches `target` (acquire).
+__device__ __forceinline__ bool counter_wait(const uint32_t* p, uint32_t target, uint32_t* ctrl,
+                                             unsigned long long timeout_ns, uint32_t site) {
+  if (ld_acquire(p) >= target) return true;
+  const uint64_t t0 = globaltimer();
+  uint32_t it = 0;
+  while (ld_acquire(p) < target) {
+    __nanosleep(64);
+    if ((++it & 15u) == 0u) {
+      if (ld_volatile(&ctrl[kAbort]) != 0u) return false;
+      if (globaltimer() - t0 > timeout_ns) {
+        set_error(ctrl, MM_ERR_TIMEOUT, site);
+        return false;
+      }
+    }
+  }
+  return true;
+}
+
+// ---- TMA (2-D tiled load into this CTA's shared memory)
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int32_t x, int32_t y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];"
+      :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// ---- cp.async (4-byte) for the scale-factor transposition
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" :: "r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
+
+// ---- tcgen05
+__device__ __forceinline__ void tc_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" :: "r"(dst_smem), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tc_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" :: "r"(bar) : "memory");
+}
+// Copy a 32-row x 16-byte scale atom from shared memory to 4 TMEM columns,
+// replicated to the four 32-lane quarters.
+__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t src_desc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" :: "r"(taddr), "l"(src_desc) : "memory");
+}
+// D (+)= (A * 2^sfa) . (B * 2^sfb)^T, block-scaled, one scale per 32 K.
+__device__ __forceinline__ void tc_mma_mx(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+      :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+// 32 lanes x 16 columns of 32-bit accumulators into registers.
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr) : "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor, K-major operand tile with 128-byte swizzle:
+// rows of 128 bytes, 8-row groups 1024 bytes apart (tile base 1 KB aligned).
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);        // start address (16-byte units)
+  d |= (uint64_t)1 << 16;                           // leading byte offset (unused for SW128 K-major)
+  d |= (uint64_t)(1024 >> 4) << 32;                 // stride byte offset: 8 rows x 128 B
+  d |= (uint64_t)1 << 46;                           // descriptor version
+  d |= (uint64_t)2 << 61;                           // 128-byte swizzle
+  return d;
+}
+// Descriptor of a dense 32-row x 16-byte scale atom (no swizzle; 8-row groups 128 B apart).
+__device__ __forceinline__ uint64_t desc_sf(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)(128 >> 4) << 16;
+  d |= (uint64_t)(128 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  return d;
+}
+// Instruction descriptor of kind::mxf8f6f4 with UE8M0 scales: A = E2M1 weights
+// (M = 128), B = E4M3 tokens (N), both K-major; sf_id selects the scale byte
+// (the 32-element K block within the 128-element stage).
+__device__ __forceinline__ uint32_t idesc_mx(uint32_t n, uint32_t sf_id) {
+  uint32_t d = 0;
+  d |= sf_id << 4;                 // B scale-factor id
+  d |= 5u << 7;                    // A format: E2M1
+  d |= 0u << 10;                   // B format: E4M3
+  d |= (n >> 3) << 17;             // N / 8
+  d |= 1u << 23;                   // scale format: UE8M0
+  d |= (128u >> 4) << 24;          // M / 16
+  d |= sf_id << 29;                // A scale-factor id
+  return d;
+}
+
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
+  asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(nthreads) : "memory");
+}
+
+#endif  // __CUDACC__
+
+}  // namespace mm

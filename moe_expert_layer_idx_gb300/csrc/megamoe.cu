@@ -1,0 +1,496 @@
+// The persistent fused MoE expert layer kernel for GB300 (sm_103a).
+//
+// One CTA per SM (grid sized by the host from the SM count minus a reserve,
+// rounded down to even -- sglang PR #36657 "[Blackwell] Reserve SMs for
+// DeepGEMM MegaMoE grid barriers", sections Root cause and Fix).  Phases:
+//
+//  0. dispatch: every warp copies expert-sorted token rows (and their UE8M0
+//     scales) into the workspace and bumps that expert's arrival counter with
+//     a release -- the "token/SF pull ... l1_arrival_count release" of the
+//     DeepGEMM SM90 MegaMoE dev log (Phase 2 entry), restricted to one GPU.
+//  1. tiles, warp-specialised, statically scheduled (tile t -> CTA t % grid):
+//       warp 0 / lane 0  TMA producer: FP4 weight rows (packed -> padded 8-bit
+//                        containers by the 16U4_ALIGN16B tensor map) and FP8
+//                        token rows, 128-byte swizzled, 4-stage ring;
+//       warp 1 / lane 0  MMA issuer: scale atoms -> TMEM (tcgen05.cp), then
+//                        4 x tcgen05.mma kind::mxf8f6f4 block_scale (K = 32
+//                        each) per stage into a double-buffered TMEM
+//                        accumulator (M = 128 weight rows, N = tokens);
+//       warp 2           scale loader: gathers the UE8M0 scale bytes of the
+//                        stage into the 32x4x4 atom layout with cp.async;
+//       warps 4-7        epilogue: tcgen05.ld the accumulator.
+//     L1 tiles (expert e, 64 intermediate features, <= 240 tokens): rows
+//     [0,64) of the tile are gate rows, [64,128) up rows; the epilogue pairs
+//     them, applies the clamp and SwiGLU, requantises each 32-feature block to
+//     E4M3 + UE8M0, writes l1_acts, and releases the expert's L1-done count.
+//     L2 tiles (expert e, 128 hidden rows) wait for that count, multiply by
+//     the token's top-k weight and write fp32 rows indexed by the flat
+//     assignment (fp32, not bf16: when a token's k contributions cancel, a
+//     bf16 rounding of each one is large next to their sum).  (Weights sit on the MMA M side and tokens on N so that a
+//     decode batch with a handful of tokens per expert wastes no tensor work.)
+//  2. whole-grid software barrier, then the combine: y[t] = bf16(sum_j of the
+//     weighted rows t*k + j, in ascending j).
+//
+// Every wait is bounded (global timer + abort flag): a wait that runs out
+// records MM_ERR_TIMEOUT with the SM and the wait site, raises the abort flag
+// and the CTA drains its own in-flight copies and MMAs, frees its TMEM and
+// returns -- the pages' kernel reports "grid sync timeout: sm=.., thread=..,
+// grid_sync_idx=.." (digest of PR #36657, 功能与动机) instead of hanging.
+// All counters are reset by the routing kernel of the same launch, never
+// keyed on %gridid (DeepGEMM PR #451).
+#include "common.cuh"
+#include "numerics.cuh"
+
+namespace mm {
+
+struct Tile {
+  int layer;   // 1 or 2
+  int e;       // expert
+  int mt;      // M block: 64-feature block (L1) or 128-row block (L2)
+  int r0;      // first slot of the N block
+  int rows;    // valid tokens in the N block
+  int n;       // MMA N (rows rounded up to 16)
+  int ks;      // K stages
+};
+
+__device__ __forceinline__ void decode_tile(int t, int nL1, const ForwardParams& p, const int32_t* items,
+                                            const int32_t* counts, const int32_t* offsets, Tile& ti) {
+  const bool l1 = t < nL1;
+  const int tt = l1 ? t : t - nL1;
+  const int MT = l1 ? p.mt1 : p.mt2;
+  int lo = 0, hi = p.E;   // largest e with items[e] * MT <= tt
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(items + mid) * MT <= tt) lo = mid; else hi = mid;
+  }
+  const int e = lo;
+  const int i0 = __ldg(items + e);
+  const int nbk = __ldg(items + e + 1) - i0;
+  const int local = tt - i0 * MT;
+  const int mt = local / nbk;
+  const int nb = local - mt * nbk;
+  const int cnt = __ldg(counts + e);
+  const int rpb = (cnt + nbk - 1) / nbk;
+  const int start = nb * rpb;
+  ti.layer = l1 ? 1 : 2;
+  ti.e = e;
+  ti.mt = mt;
+  ti.r0 = __ldg(offsets + e) + start;
+  ti.rows = min(rpb, cnt - start);
+  ti.n = (ti.rows + 15) & ~15;
+  ti.ks = l1 ? p.ks1 : p.ks2;
+}
+
+__device__ __forceinline__ uint32_t l1_tiles_of(const int32_t* items, int e, int mt1) {
+  return (uint32_t)((__ldg(items + e + 1) - __ldg(items + e)) * mt1);
+}
+
+__device__ __forceinline__ uint16_t bf16_bits_rn(float v) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+}
+
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" :: "r"(bar) : "memory");
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant__ CUtensorMap tm_w2,
+               const __grid_constant__ CUtensorMap tm_xs, const __grid_constant__ CUtensorMap tm_l1a,
+               const __grid_constant__ ForwardParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = sm;
+  uint8_t* sB = sA + kStages * kABytes;
+  uint8_t* sSFA = sB + kStages * kBBytes;
+  uint8_t* sSFB = sSFA + kStages * kSFABytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sSFB + kStages * kSFBBytes);
+  uint64_t* full_tma = bars;                 // [kStages] TMA bytes landed
+  uint64_t* full_sf = bars + kStages;        // [kStages] 32 scale-loader lanes' cp.async landed
+  uint64_t* empty = bars + 2 * kStages;      // [kStages] MMAs reading the stage are done
+  uint64_t* tfull = bars + 3 * kStages;      // [2] accumulator ready
+  uint64_t* tempty = tfull + 2;              // [2] accumulator drained (4 epilogue warps)
+  uint64_t* drain = tempty + 2;              // [1] final MMA drain
+  uint32_t* s_misc = reinterpret_cast<uint32_t*>(drain + 1);   // tmem base, consumed, issued, combine-off
+  int32_t* s_vote = reinterpret_cast<int32_t*>(s_misc + 4);    // epilogue votes [2][4]
+  float* xchg = reinterpret_cast<float*>(sm + kStages * kStageBytes + 256);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint32_t* ctrl = reinterpret_cast<uint32_t*>(p.ws + p.L.ctrl);
+  if (ld_volatile(&ctrl[kStatus]) != 0u) return;   // routing rejected the input
+
+  const int32_t* counts = reinterpret_cast<const int32_t*>(p.ws + p.L.counts);
+  const int32_t* offsets = reinterpret_cast<const int32_t*>(p.ws + p.L.offsets);
+  const int32_t* items = reinterpret_cast<const int32_t*>(p.ws + p.L.items);
+  uint32_t* arrival = reinterpret_cast<uint32_t*>(p.ws + p.L.arrival);
+  uint32_t* l1_done = reinterpret_cast<uint32_t*>(p.ws + p.L.l1_done);
+  const int32_t* perm = reinterpret_cast<const int32_t*>(p.ws + p.L.perm);
+  uint8_t* xs = p.ws + p.L.xs;
+  uint8_t* xs_sf = p.ws + p.L.xs_sf;
+  uint8_t* l1a = p.ws + p.L.l1a;
+  uint8_t* l1a_sf = p.ws + p.L.l1a_sf;
+  float* stage_out = reinterpret_cast<float*>(p.ws + p.L.stage);
+  const unsigned long long to = p.timeout_ns;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full_tma[s], 1);
+      mbar_init(&full_sf[s], 32);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 4);
+    }
+    mbar_init(drain, 1);
+    s_misc[1] = 0; s_misc[2] = 0; s_misc[3] = 0;
+    fence_mbar_init();
+    prefetch_tensormap(&tm_w1);
+    prefetch_tensormap(&tm_w2);
+    prefetch_tensormap(&tm_xs);
+    prefetch_tensormap(&tm_l1a);
+  }
+  if (warp == 1) {
+    tc_alloc(smem_u32(&s_misc[0]), kTmemCols);
+    tc_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_misc[0];
+
+  // ------------------------------------------------------------ 0. dispatch
+  {
+    const int nvalid = __ldg(offsets + p.E);
+    const int H = p.H;
+    const int nvec = H / 16, nsf = H / 128;
+    for (int s = blockIdx.x * (kThreads / 32) + warp; s < nvalid; s += gridDim.x * (kThreads / 32)) {
+      const int f = __ldg(perm + s);
+      const int t = f / p.k;
+      const int e = __ldg(p.topk_idx + f);
+      const uint4* src = reinterpret_cast<const uint4*>(p.x + (size_t)t * H);
+      uint4* dst = reinterpret_cast<uint4*>(xs + (size_t)s * H);
+      for (int c = lane; c < nvec; c += 32) dst[c] = __ldg(src + c);
+      const uint32_t* ssf = reinterpret_cast<const uint32_t*>(p.x_sf + (size_t)t * (H / 32));
+      uint32_t* dsf = reinterpret_cast<uint32_t*>(xs_sf + (size_t)s * (H / 32));
+      for (int c = lane; c < nsf; c += 32) dsf[c] = __ldg(ssf + c);
+      fence_proxy_async_global();
+      __threadfence();
+      __syncwarp();
+      if (lane == 0) red_release_add(&arrival[e], 1u);
+    }
+  }
+
+  const int nItems = __ldg(items + p.E);
+  const int nL1 = nItems * p.mt1;
+  const int total = nL1 + nItems * p.mt2;
+
+  // ------------------------------------------------------------ 1. tiles
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer
+      uint32_t stage = 0, phase = 0, issued = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        Tile ti;
+        decode_tile(t, nL1, p, items, counts, offsets, ti);
+        const uint32_t tag = (uint32_t)t & 0xFFFFFFu;
+        if (ti.layer == 1)
+          ok = counter_wait(&arrival[ti.e], (uint32_t)__ldg(counts + ti.e), ctrl, to, (kSiteArrival << 24) | tag);
+        else
+          ok = counter_wait(&l1_done[ti.e], l1_tiles_of(items, ti.e, p.mt1), ctrl, to, (kSiteL1Done << 24) | tag);
+        if (!ok) break;
+        fence_proxy_async_global();
+        const uint32_t bytes = (uint32_t)(kATxBytes + ti.n * kBlockK);
+        for (int kb = 0; kb < ti.ks; ++kb) {
+          if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, ctrl, to, (kSiteEmpty << 24) | tag)) { ok = false; break; }
+          const uint32_t fb = smem_u32(&full_tma[stage]);
+          mbar_arrive_expect_tx(fb, bytes);
+          const uint32_t a_dst = smem_u32(sA + stage * kABytes);
+          const uint32_t b_dst = smem_u32(sB + stage * kBBytes);
+          const int kx = kb * kBlockK;
+          if (ti.layer == 1) {
+            const int row = ti.e * 2 * p.I + ti.mt * kL1Feat;
+            tma_load_2d(a_dst, &tm_w1, fb, kx, row);                             // gate rows
+            tma_load_2d(a_dst + kL1Feat * kBlockK, &tm_w1, fb, kx, row + p.I);   // up rows
+            for (int j = 0; j < ti.n / 16; ++j)
+              tma_load_2d(b_dst + j * 16 * kBlockK, &tm_xs, fb, kx, ti.r0 + 16 * j);
+          } else {
+            const int row = ti.e * p.H + ti.mt * kL2Rows;
+            tma_load_2d(a_dst, &tm_w2, fb, kx, row);
+            for (int j = 0; j < ti.n / 16; ++j)
+              tma_load_2d(b_dst + j * 16 * kBlockK, &tm_l1a, fb, kx, ti.r0 + 16 * j);
+          }
+          ++issued;
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+      }
+      s_misc[2] = issued;
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer
+      uint32_t stage = 0, phase = 0, ab = 0, aphase = 0, consumed = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        Tile ti;
+        decode_tile(t, nL1, p, items, counts, offsets, ti);
+        const uint32_t tag = (uint32_t)t & 0xFFFFFFu;
+        if (!mbar_wait(smem_u32(&tempty[ab]), aphase ^ 1u, ctrl, to, (kSiteTmemEmpty << 24) | tag)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + ab * kAccStride;
+        for (int kb = 0; kb < ti.ks; ++kb) {
+          if (!mbar_wait(smem_u32(&full_tma[stage]), phase, ctrl, to, (kSiteFull << 24) | tag) ||
+              !mbar_wait(smem_u32(&full_sf[stage]), phase, ctrl, to, (kSiteFullSf << 24) | tag)) { ok = false; break; }
+          tc_fence_after();
+          fence_proxy_async_shared();   // scale atoms were written through the generic proxy
+          const uint32_t sfa = smem_u32(sSFA + stage * kSFABytes);
+          const uint32_t sfb = smem_u32(sSFB + stage * kSFBBytes);
+          tc_cp_sf(tmem + kSFACol, desc_sf(sfa));
+          tc_cp_sf(tmem + kSFBCol, desc_sf(sfb));
+          if (ti.n > 128) tc_cp_sf(tmem + kSFBCol + 4, desc_sf(sfb + 512));
+          const uint32_t a0 = smem_u32(sA + stage * kABytes);
+          const uint32_t b0 = smem_u32(sB + stage * kBBytes);
+#pragma unroll
+          for (int kk = 0; kk < kBlockK / 32; ++kk) {
+            tc_mma_mx(d_tmem, desc_sw128(a0 + kk * 32), desc_sw128(b0 + kk * 32), idesc_mx((uint32_t)ti.n, (uint32_t)kk),
+                      tmem + kSFACol, tmem + kSFBCol, (kb | kk) != 0 ? 1u : 0u);
+          }
+          tc_commit(smem_u32(&empty[stage]));
+          ++consumed;
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        tc_commit(smem_u32(&tfull[ab]));
+        ab ^= 1u;
+        if (ab == 0) aphase ^= 1u;
+      }
+      s_misc[1] = consumed;
+      tc_commit(smem_u32(drain));
+      mbar_wait(smem_u32(drain), 0, ctrl, to, kSiteDrain << 24);
+    }
+  } else if (warp == 2) {
+    // ---------------- scale loader (32 lanes)
+    uint32_t stage = 0, phase = 0;
+    const int H32 = p.H / 32, I32 = p.I / 32;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      Tile ti;
+      decode_tile(t, nL1, p, items, counts, offsets, ti);
+      const uint32_t tag = (uint32_t)t & 0xFFFFFFu;
+      bool ok = true;
+      if (lane == 0) {
+        ok = (ti.layer == 1)
+                 ? counter_wait(&arrival[ti.e], (uint32_t)__ldg(counts + ti.e), ctrl, to, (kSiteArrival << 24) | tag)
+                 : counter_wait(&l1_done[ti.e], l1_tiles_of(items, ti.e, p.mt1), ctrl, to, (kSiteL1Done << 24) | tag);
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      __syncwarp();
+      // every lane acquires the producers' writes before reading them
+      if (ti.layer == 1) (void)ld_acquire(&arrival[ti.e]); else (void)ld_acquire(&l1_done[ti.e]);
+      const uint8_t* a_sf_base;
+      int a_stride, a_row0, a_row_up;
+      const uint8_t* b_sf_base;
+      int b_stride;
+      if (ti.layer == 1) {
+        a_sf_base = p.w1_sf; a_stride = H32;
+        a_row0 = ti.e * 2 * p.I + ti.mt * kL1Feat; a_row_up = a_row0 + p.I - kL1Feat;
+        b_sf_base = xs_sf; b_stride = H32;
+      } else {
+        a_sf_base = p.w2_sf; a_stride = I32;
+        a_row0 = ti.e * p.H + ti.mt * kL2Rows; a_row_up = a_row0;
+        b_sf_base = l1a_sf; b_stride = I32;
+      }
+      for (int kb = 0; kb < ti.ks; ++kb) {
+        bool w = true;
+        if (lane == 0) w = mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, ctrl, to, (kSiteEmpty << 24) | tag);
+        w = __shfl_sync(0xffffffffu, w, 0);
+        if (!w) { ok = false; break; }
+        const uint32_t dA = smem_u32(sSFA + stage * kSFABytes) + lane * 16;
+        const uint32_t dB = smem_u32(sSFB + stage * kSFBBytes) + lane * 16;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int m = lane + 32 * j;
+          const int row = (m < kL1Feat) ? a_row0 + m : a_row_up + m;
+          cp_async_4(dA + j * 4, a_sf_base + (size_t)row * a_stride + kb * 4);
+        }
+#pragma unroll
+        for (int at = 0; at < 2; ++at) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int n = 128 * at + 32 * j + lane;
+            if (n < ti.n) {
+              const int slot = min(ti.r0 + n, p.A - 1);
+              cp_async_4(dB + at * 512 + j * 4, b_sf_base + (size_t)slot * b_stride + kb * 4);
+            }
+          }
+        }
+        cp_async_mbar_arrive_noinc(smem_u32(&full_sf[stage]));
+        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+      }
+      if (!ok) break;
+    }
+    cp_async_wait<0>();
+  } else if (warp >= 4) {
+    // ---------------- epilogue (warps 4..7 own TMEM lanes 32q .. 32q+31)
+    const int q = warp - 4;
+    uint32_t ab = 0, aphase = 0;
+    int vote_buf = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      Tile ti;
+      decode_tile(t, nL1, p, items, counts, offsets, ti);
+      const uint32_t tag = (uint32_t)t & 0xFFFFFFu;
+      bool ok = true;
+      if (lane == 0) ok = mbar_wait(smem_u32(&tfull[ab]), aphase, ctrl, to, (kSiteTmemFull << 24) | tag);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      // the four epilogue warps decide together, so none waits alone on a named barrier
+      if (lane == 0) s_vote[vote_buf * 4 + q] = ok ? 1 : 0;
+      named_bar_sync(3, 128);
+      const bool all_ok = s_vote[vote_buf * 4 + 0] & s_vote[vote_buf * 4 + 1] &
+                          s_vote[vote_buf * 4 + 2] & s_vote[vote_buf * 4 + 3];
+      vote_buf ^= 1;
+      if (!all_ok) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + ab * kAccStride;
+      if (ti.layer == 1) {
+        // ---- L1: pair gate (warps 0,1) with up (warps 2,3); SwiGLU; E4M3 requant
+        const int pair = q & 1;
+        const bool is_gate = q < 2;
+        float* xg = xchg + pair * 512;      // gate values of columns 8..15 [8][32]
+        float* xu = xg + 256;               // up values of columns 0..7   [8][32]
+        const int feat = ti.mt * kL1Feat + pair * 32 + lane;
+        const int sf_col = ti.mt * (kL1Feat / 32) + pair;
+        const float L = p.clamp;
+        for (int c0 = 0; c0 < ti.n; c0 += 16) {
+          float v[16];
+          tc_ld16(tbase + (uint32_t)c0, v);
+          tc_wait_ld();
+          if (is_gate) {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) xg[c * 32 + lane] = v[8 + c];
+          } else {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) xu[c * 32 + lane] = v[c];
+          }
+          named_bar_sync(1 + pair, 64);
+          float g[8], u[8];
+          if (is_gate) {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) { g[c] = v[c]; u[c] = xu[c * 32 + lane]; }
+          } else {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) { g[c] = xg[c * 32 + lane]; u[c] = v[8 + c]; }
+          }
+          named_bar_sync(1 + pair, 64);
+          const int cb = c0 + (is_gate ? 0 : 8);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const int col = cb + c;
+            if (col >= ti.rows) break;
+            float gg = g[c], uu = u[c];
+            if (p.use_clamp) {
+              gg = fminf(gg, L);
+              uu = fminf(fmaxf(uu, -L), L);
+            }
+            const float h = gg / (1.0f + __expf(-gg)) * uu;
+            float a = fabsf(h);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+            const int s = block_scale_exp<true>(a);
+            const uint32_t code = e4m3_code(h * exp2_neg(s));
+            const size_t slot = (size_t)(ti.r0 + col);
+            l1a[slot * p.I + feat] = (uint8_t)code;
+            if (lane == 0) l1a_sf[slot * (p.I / 32) + sf_col] = (uint8_t)(s + 127);
+          }
+        }
+      } else {
+        // ---- L2: weight by topk_w, bf16 rows indexed by the flat assignment
+        const int hrow = ti.mt * kL2Rows + q * 32 + lane;
+        for (int c0 = 0; c0 < ti.n; c0 += 16) {
+          float v[16];
+          tc_ld16(tbase + (uint32_t)c0, v);
+          tc_wait_ld();
+          const int mc = c0 + (lane & 15);
+          int f = 0;
+          float w = 0.f;
+          if (mc < ti.rows) {
+            f = __ldg(perm + ti.r0 + mc);
+            w = __ldg(p.topk_w + f);
+          }
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            if (c0 + c >= ti.rows) break;
+            const int fc = __shfl_sync(0xffffffffu, f, c);
+            const float wc = __shfl_sync(0xffffffffu, w, c);
+            stage_out[(size_t)fc * p.H + hrow] = v[c] * wc;
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&tempty[ab]));
+      if (ti.layer == 1) {
+        fence_proxy_async_global();
+        __threadfence();
+        named_bar_sync(3, 128);
+        if (q == 0 && lane == 0) red_release_add(&l1_done[ti.e], 1u);
+      }
+      ab ^= 1u;
+      if (ab == 0) aphase ^= 1u;
+    }
+    __threadfence();
+  }
+
+  // ------------------------------------------------------------ teardown
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    // after an abort, TMA loads may still be landing: wait for each issued stage
+    const uint32_t issued = s_misc[2], consumed = s_misc[1];
+    for (uint32_t s = consumed; s < issued; ++s)
+      mbar_wait(smem_u32(&full_tma[s % kStages]), (s / kStages) & 1u, ctrl, to, kSiteDrain << 24);
+  }
+  if (warp == 1) {
+    tc_fence_after();
+    tc_dealloc(tmem, kTmemCols);
+  }
+
+  // ------------------------------------------------------------ 2. grid barrier + combine
+  if (threadIdx.x == 0) {
+    __threadfence();
+    bool fine = ld_volatile(&ctrl[kAbort]) == 0u;
+    if (fine) {
+      red_release_add(&ctrl[kGridBar], 1u);
+      fine = counter_wait(&ctrl[kGridBar], gridDim.x, ctrl, to, kSiteGridBar << 24);
+    }
+    s_misc[3] = fine ? 0u : 1u;
+  }
+  __syncthreads();
+  if (s_misc[3] != 0u) return;
+
+  const int H = p.H, k = p.k;
+  const int nchunk = H / 8;
+  for (int t = blockIdx.x * (kThreads / 32) + warp; t < p.T; t += gridDim.x * (kThreads / 32)) {
+    const int idx = lane < k ? __ldg(p.topk_idx + (size_t)t * k + lane) : -1;
+    const unsigned valid = __ballot_sync(0xffffffffu, idx >= 0);
+    const float4* rows = reinterpret_cast<const float4*>(stage_out + (size_t)t * k * H);
+    uint4* yrow = reinterpret_cast<uint4*>(p.y + (size_t)t * H);
+    for (int c = lane; c < nchunk; c += 32) {
+      float acc[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+      for (int j = 0; j < k; ++j) {
+        if (!((valid >> j) & 1u)) continue;
+        const float4 a = __ldcg(rows + (size_t)j * (H / 4) + 2 * c);
+        const float4 b = __ldcg(rows + (size_t)j * (H / 4) + 2 * c + 1);
+        acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+        acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+      }
+      uint32_t o[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        o[i] = (uint32_t)bf16_bits_rn(acc[2 * i]) | ((uint32_t)bf16_bits_rn(acc[2 * i + 1]) << 16);
+      yrow[c] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
+}
+
+}  // namespace mm

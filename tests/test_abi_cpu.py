@@ -1,0 +1,168 @@
+"""Host-side checks of the C ABI, no GPU needed: the library builds and loads,
+exports every entry point declared in include/*.h, rejects bad arguments
+before touching the device, and sizes the persistent grid as the pages do."""
+import glob
+import math
+import os
+import re
+
+import pytest
+
+import moe_expert_layer_idx_gb300 as mm
+from moe_expert_layer_idx_gb300 import build as mmbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    mmbuild.build()
+    return mm.lib()
+
+
+def _declared():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"\b(mm_[a-z0-9_]+)\s*\(", text):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+def test_header_declares_the_abi():
+    names = _declared()
+    for want in ("mm_workspace_size", "mm_forward", "mm_set_reserved_sms"):
+        assert want in names
+
+
+def test_exports_every_declared_symbol(lib):
+    missing = [n for n in _declared() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+# ---------------------------------------------------------------- launch size
+def _pages_rule(device_sms, reserve, current):
+    """The SM-reserve arithmetic of sglang PR #36657 (digest page, 关键源码片段):
+    max_num_sms = max(2, physical - max(reserve, 0)); target = min(max, current);
+    target -= target % 2."""
+    max_num = max(2, device_sms - max(reserve, 0))
+    target = min(max_num, current)
+    target -= target % 2
+    return target
+
+
+@pytest.mark.parametrize("sms", [148, 152, 160, 7])
+@pytest.mark.parametrize("reserve", [-3, 0, 1, 2, 3, 10, 500])
+@pytest.mark.parametrize("current", [0, 1, 2, 3, 75, 150, 151, 152, 1000])
+def test_grid_size_follows_the_pages(lib, sms, reserve, current):
+    got = mm.mm_grid_size(sms, reserve, current, 0)
+    cur = min(current, sms) if current > 0 else sms
+    want = _pages_rule(sms, reserve, cur)
+    assert got == max(want, 2)          # our floor: never fewer than one 2-CTA pair
+    assert got % 2 == 0
+
+
+def test_grid_size_examples(lib):
+    assert mm.mm_grid_size(152, 2, 0, 0) == 150      # default reserve of two
+    assert mm.mm_grid_size(152, 0, 0, 0) == 152      # reserve disabled
+    assert mm.mm_grid_size(152, 1, 0, 0) == 150      # odd -> even
+    assert mm.mm_grid_size(152, 400, 0, 0) == 2      # excessive reserve floors at 2
+    assert mm.mm_grid_size(152, 2, 0, 140) == 140    # never more CTAs than can be resident
+    assert mm.mm_grid_size(152, 2, 0, 141) == 140
+    assert mm.mm_grid_size(1, 0, 0, 0) == mm.MM_ERR_INVALID_ARG
+
+
+def test_reserved_sms_setting(lib):
+    prev = mm.mm_get_reserved_sms()
+    if "MM_RESERVED_SMS" not in os.environ:
+        assert prev == 2
+    try:
+        assert mm.mm_set_reserved_sms(-4) == prev
+        assert mm.mm_get_reserved_sms() == 0
+        assert mm.mm_set_reserved_sms(6) == 0
+        assert mm.mm_get_reserved_sms() == 6
+    finally:
+        mm.mm_set_reserved_sms(prev)
+
+
+def test_wait_timeout_setting(lib):
+    prev = mm.mm_get_wait_timeout_ns()
+    try:
+        mm.mm_set_wait_timeout_ns(12345)
+        assert mm.mm_get_wait_timeout_ns() == 12345
+        mm.mm_set_wait_timeout_ns(0)
+        assert mm.mm_get_wait_timeout_ns() == 2_000_000_000
+    finally:
+        mm.mm_set_wait_timeout_ns(prev)
+
+
+# ---------------------------------------------------------------- workspace
+def test_workspace_size_depends_on_shape_only(lib):
+    a = mm.mm_workspace_size(128, 256, 8, 7168, 2048)
+    assert a > 0
+    assert mm.mm_workspace_size(129, 256, 8, 7168, 2048) > a
+    # the dispatched tokens, L1 activations and weighted L2 rows dominate
+    A = 128 * 8
+    assert a >= A * (7168 + 7168 // 32 + 2048 + 2048 // 32 + 4 * 7168)
+    assert a < A * (7168 + 7168 // 32 + 2048 + 2048 // 32 + 4 * 7168) + 64 * 1024
+
+
+@pytest.mark.parametrize("args", [(16, 8, 2, 100, 128), (16, 8, 2, 256, 64), (16, 0, 2, 256, 128),
+                                  (16, 8, 17, 256, 128), (16, 1025, 2, 256, 128), (-1, 8, 2, 256, 128)])
+def test_workspace_size_rejects_unsupported(lib, args):
+    assert mm.mm_workspace_size(*args) == 0
+
+
+def test_workspace_regions_are_disjoint_and_aligned(lib):
+    shape = (100, 16, 4, 512, 256)
+    total = mm.mm_workspace_size(*shape)
+    end = 0
+    for name in mm.REGIONS:
+        off, nb = mm.mm_workspace_region(name, *shape)
+        assert off % 256 == 0 and off >= end
+        end = off + nb
+    assert end <= total
+
+
+# ---------------------------------------------------------------- argument errors
+FAKE = 1 << 20        # an aligned address that is never dereferenced
+
+
+def _fwd(**kw):
+    a = dict(num_tokens=64, experts=8, topk=2, hidden=256, inter=128, x=FAKE, x_sf=FAKE, topk_idx=FAKE,
+             topk_w=FAKE, l1_w=FAKE, l1_sf=FAKE, l2_w=FAKE, l2_sf=FAKE, y=FAKE, clamp=7.0, num_sms=0,
+             workspace=FAKE, workspace_bytes=1 << 40, stream=0)
+    a.update(kw)
+    return mm.mm_forward(**a)
+
+
+def test_forward_argument_errors(lib):
+    assert _fwd(num_tokens=0) == mm.MM_OK                      # nothing to do, nothing launched
+    assert _fwd(hidden=200) == mm.MM_ERR_UNSUPPORTED_SHAPE
+    assert _fwd(inter=192) == mm.MM_ERR_UNSUPPORTED_SHAPE
+    assert _fwd(topk=17) == mm.MM_ERR_UNSUPPORTED_SHAPE
+    assert _fwd(experts=0) == mm.MM_ERR_INVALID_ARG
+    assert _fwd(x=0) == mm.MM_ERR_INVALID_ARG
+    assert _fwd(y=0) == mm.MM_ERR_INVALID_ARG
+    assert _fwd(x=FAKE + 8) == mm.MM_ERR_INVALID_ARG            # x needs 16-byte alignment
+    assert _fwd(l1_w=FAKE + 16) == mm.MM_ERR_INVALID_ARG        # packed FP4 weights need 32
+    assert _fwd(workspace=FAKE + 128) == mm.MM_ERR_INVALID_ARG  # workspace needs 256
+    assert _fwd(clamp=math.nan) == mm.MM_ERR_INVALID_ARG
+    need = mm.mm_workspace_size(64, 8, 2, 256, 128)
+    assert _fwd(workspace_bytes=need - 1) == mm.MM_ERR_WORKSPACE_TOO_SMALL
+
+
+def test_route_and_quantize_argument_errors(lib):
+    assert mm.mm_route(64, 8, 2, 256, 128, FAKE, FAKE, 10, 0) == mm.MM_ERR_WORKSPACE_TOO_SMALL
+    assert mm.mm_route(64, 8, 2, 256, 128, 0, FAKE, 1 << 40, 0) == mm.MM_ERR_INVALID_ARG
+    assert mm.mm_quantize_mx(FAKE, 4, 48, mm.MM_FMT_E4M3, FAKE, FAKE, 0) == mm.MM_ERR_INVALID_ARG
+    assert mm.mm_quantize_mx(FAKE, 4, 64, 7, FAKE, FAKE, 0) == mm.MM_ERR_INVALID_ARG
+    assert mm.mm_quantize_mx(FAKE, 0, 64, mm.MM_FMT_E4M3, FAKE, FAKE, 0) == mm.MM_OK
+
+
+def test_forward_without_device(lib):
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert _fwd() == mm.MM_ERR_NO_DEVICE

@@ -1,0 +1,62 @@
+"""Routing kernel against the oracle: counts, offsets, permutation and its
+inverse bit-exact (the stable order makes them unique)."""
+import numpy as np
+import pytest
+import torch
+
+import moe_expert_layer_idx_gb300 as mm
+import synth
+from oracle.routing import route
+
+pytestmark = pytest.mark.gpu
+
+
+def _gpu_route(idx: np.ndarray, E: int, H=256, I=128):
+    T, k = idx.shape
+    ws = torch.empty(mm.mm_workspace_size(max(T, 1), E, k, H, I), dtype=torch.uint8, device="cuda")
+    d_idx = torch.from_numpy(np.ascontiguousarray(idx, np.int32)).cuda()
+    assert mm.mm_route(T, E, k, H, I, d_idx, ws) == mm.MM_OK
+    st = mm.mm_get_status(ws)
+    rc, counts, offsets, perm, inv = mm.mm_read_routing(T, E, k, H, I, ws)
+    assert rc == mm.MM_OK
+    return st, counts, offsets, perm, inv
+
+
+def _check(idx, E):
+    st, c, o, p, i = _gpu_route(idx, E)
+    assert st[0] == mm.MM_OK
+    rc, ro, rp, ri = route(idx, E)
+    n = int(ro[-1])
+    assert np.array_equal(c, rc)
+    assert np.array_equal(o, ro)
+    assert np.array_equal(p[:n], rp)
+    assert np.array_equal(i, ri)
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode", "prefill", "skew", "kimi"])
+def test_routing_of_the_configs(name):
+    cfg = synth.CONFIGS[name]
+    idx, _, _ = synth.routing(cfg)
+    _check(idx, cfg.E)
+
+
+@pytest.mark.parametrize("T,E,k,empty", [(1, 1, 1, 0.0), (8, 4, 3, 0.0), (48, 16, 2, 0.3), (192, 1024, 16, 0.1),
+                                         (33, 7, 5, 0.0), (1000, 3, 1, 0.5), (5, 1024, 1, 0.0)])
+def test_routing_edge_shapes(T, E, k, empty):
+    rng = np.random.default_rng(T + E + k)
+    idx = rng.integers(0, E, (T, k)).astype(np.int32)          # duplicate experts per token allowed
+    idx[rng.random((T, k)) < empty] = -1
+    _check(idx, E)
+
+
+def test_all_slots_empty():
+    _check(np.full((40, 4), -1, np.int32), 8)
+
+
+def test_bad_index_is_reported():
+    idx = np.zeros((20, 2), np.int32)
+    idx[7, 1] = 8          # E = 8 -> out of range
+    idx[12, 0] = -3
+    st, *_ = _gpu_route(idx, 8)
+    assert st[0] == mm.MM_ERR_BAD_INDEX
+    assert st[2] == 7 * 2 + 1   # first bad flat index
