@@ -58,10 +58,14 @@ def _peaks():
         return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
 
 
+KERNEL_SOURCES = ("megamoe.cu", "common.cuh", "numerics.cuh")
+
+
 def _kernel_source_hash():
+    """Hash of the persistent layer kernel's sources (profiles are tied to it)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "moe_expert_layer_idx_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in KERNEL_SOURCES:
         with open(os.path.join(csrc, name), "rb") as fh:
             h.update(name.encode())
             h.update(fh.read())
@@ -312,7 +316,9 @@ def run_oracle_sample(workload, sample_tokens, time_budget_s=25.0):
     toks = list(range(min(n, cfg.T)))
     xc, xsf = OF.quantize_mx(synth.x_f32(cfg, rows=toks), OF.E4M3)
     experts = sorted({int(e) for e in idx[toks].reshape(-1) if e >= 0})
+    tp = time.perf_counter()
     cache = {e: OM.quantize_expert(synth.w1_f32(cfg, e), synth.w2_f32(cfg, e)) for e in experts}
+    _log(f"oracle sample: {len(experts)} experts prepared in {time.perf_counter() - tp:.1f} s")
     t0 = time.perf_counter()
     OM.moe_forward(xc, xsf, idx[toks], w[toks], lambda e: cache[e], cfg.clamp, cfg.E)
     dt = time.perf_counter() - t0
@@ -330,7 +336,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode")
-    ap.add_argument("--cpu-sample-tokens", type=int, default=1)
+    ap.add_argument("--cpu-sample-tokens", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tokens", type=int, default=0, help="override the token count (profiling of small cases)")
     ap.add_argument("--experts", type=int, default=0, help="override the expert count (profiling of small cases)")
