@@ -220,6 +220,37 @@ int mm_workspace_region(int which, int num_tokens, int experts, int topk, int hi
 int mm_quantize_mx(const float* src, long long rows, long long cols, int fmt,
                    void* dst, void* dst_sf, mm_stream_t stream);
 
+/*
+ * mm_forward_noalloc -- mm_forward without a caller-provided workspace.  The
+ * pages have no counterpart to this entry point.
+ *
+ * Some callers cannot allocate device memory at the point where they run the
+ * layer: code running while a stream is being captured into a CUDA graph
+ * (cudaMalloc is not permitted during capture), inference runtimes whose
+ * device memory is entirely owned by their own pool allocator, and real-time
+ * loops that forbid allocation after start-up.  For them the library keeps
+ * one fixed scratch array of 48 MiB in device memory (a file-scope __device__
+ * array, present on every GPU where the library's kernels are loaded until
+ * the process exits), enough for a decode batch of the DeepSeek-sized layer
+ * (128 tokens, top-8, hidden 7168, inter 2048 needs 39 MB).
+ *
+ * Arguments are those of mm_forward minus the workspace.  A shape whose
+ * workspace (mm_workspace_size) exceeds 48 MiB is rejected with
+ * MM_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.  No cudaMalloc,
+ * cudaFree or allocating routine is called.  The first call on a device looks
+ * up the array's device address (cudaGetSymbolAddress, with that device
+ * current); make that first call before any stream capture.  Every call on a
+ * device shares the same array, and each launch resets what must start at
+ * zero; two calls whose kernels overlap on the GPU (different streams, or
+ * different host threads) race on it.  Device-side errors are recorded in the
+ * array's status word, which mm_get_status cannot reach: after such an error
+ * the output is undefined, and the next call resets the status.
+ */
+int mm_forward_noalloc(int num_tokens, int experts, int topk, int hidden, int inter,
+                       const void* x, const void* x_sf, const int32_t* topk_idx, const float* topk_w,
+                       const void* l1_w, const void* l1_sf, const void* l2_w, const void* l2_sf,
+                       void* y, float clamp, int num_sms, mm_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

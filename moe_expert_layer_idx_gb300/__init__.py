@@ -49,6 +49,7 @@ _SIGS = {
     "mm_read_routing": (_c_int, [_c_int] * 5 + [_c_vp] * 5),
     "mm_workspace_region": (_c_int, [_c_int] * 6 + [_c_vp, _c_vp]),
     "mm_quantize_mx": (_c_int, [_c_vp, _c_ll, _c_ll, _c_int, _c_vp, _c_vp, _c_vp]),
+    "mm_forward_noalloc": (_c_int, [_c_int] * 5 + [_c_vp] * 9 + [ctypes.c_float, _c_int, _c_vp]),
 }
 
 
@@ -167,6 +168,15 @@ def mm_workspace_region(which, num_tokens, experts, topk, hidden, inter):
 
 def mm_quantize_mx(src, rows, cols, fmt, dst, dst_sf, stream=None) -> int:
     return lib().mm_quantize_mx(_ptr(src), rows, cols, fmt, _ptr(dst), _ptr(dst_sf), _stream(stream))
+
+
+def mm_forward_noalloc(num_tokens, experts, topk, hidden, inter, x, x_sf, topk_idx, topk_w, l1_w, l1_sf,
+                       l2_w, l2_sf, y, clamp, num_sms, stream=None) -> int:
+    """mm_forward with the library's fixed 48 MiB device scratch as workspace,
+    for callers that cannot allocate device memory (see include/megamoe.h)."""
+    return lib().mm_forward_noalloc(num_tokens, experts, topk, hidden, inter, _ptr(x), _ptr(x_sf),
+                                    _ptr(topk_idx), _ptr(topk_w), _ptr(l1_w), _ptr(l1_sf), _ptr(l2_w),
+                                    _ptr(l2_sf), _ptr(y), float(clamp), num_sms, _stream(stream))
 
 
 # ------------------------------------------------------------------ convenience

@@ -9,7 +9,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libmegamoe.so")
-SOURCES = ["api.cu", "route.cu", "megamoe.cu", "quant.cu"]
+SOURCES = ["api.cu", "route.cu", "megamoe.cu", "quant.cu", "noalloc.cu"]
 HEADERS = ["common.cuh", "numerics.cuh"]
 ARCH = "103a"
 

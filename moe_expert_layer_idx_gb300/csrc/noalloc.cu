@@ -1,0 +1,57 @@
+// mm_forward_noalloc: the fused layer with its workspace in a fixed device
+// array that the library owns, for callers that cannot allocate device
+// memory themselves (see include/megamoe.h for who they are and why).
+//
+// The scratch array below is a file-scope __device__ variable: it exists on
+// every GPU where this library's kernels are loaded and stays there until the
+// process exits.  In host code its name is only a host-side stand-in, never a
+// device address, so the device address is looked up once per device with
+// cudaGetSymbolAddress (with that device current) and passed to the kernels
+// as an ordinary workspace pointer.
+#include <mutex>
+
+#include "common.cuh"
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = 48ull << 20;   // 48 MiB
+
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[128] = {};   // device address of the array, per device ordinal
+
+}  // namespace
+
+extern "C" int mm_forward_noalloc(int num_tokens, int experts, int topk, int hidden, int inter,
+                                  const void* x, const void* x_sf, const int32_t* topk_idx, const float* topk_w,
+                                  const void* l1_w, const void* l1_sf, const void* l2_w, const void* l2_sf,
+                                  void* y, float clamp, int num_sms, mm_stream_t stream) {
+  const size_t need = mm_workspace_size(num_tokens, experts, topk, hidden, inter);
+  if (need == 0) {
+    // unsupported dimensions: let mm_forward report the precise reason
+    return mm_forward(num_tokens, experts, topk, hidden, inter, x, x_sf, topk_idx, topk_w, l1_w, l1_sf, l2_w,
+                      l2_sf, y, clamp, num_sms, nullptr, 0, stream);
+  }
+  if (need > kNoAllocScratchBytes) return MM_ERR_WORKSPACE_TOO_SMALL;   // beyond the fixed scratch
+  if (num_tokens == 0) return MM_OK;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return MM_ERR_NO_DEVICE; }
+  if (dev < 0 || dev >= 128) return MM_ERR_NO_DEVICE;
+  void* ws = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+        cudaGetLastError();
+        return MM_ERR_CUDA;
+      }
+      g_noalloc_ptr[dev] = p;
+    }
+    ws = g_noalloc_ptr[dev];
+  }
+  return mm_forward(num_tokens, experts, topk, hidden, inter, x, x_sf, topk_idx, topk_w, l1_w, l1_sf, l2_w, l2_sf,
+                    y, clamp, num_sms, ws, kNoAllocScratchBytes, stream);
+}
