@@ -138,6 +138,15 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def replica_throughput(ms_local, tokens_per_rank, world, max_over_ranks):
+    """Whole-job throughput of `world` independent replicas: every rank ran
+    `tokens_per_rank` tokens per step; the job's step time is the slowest
+    rank's.  `max_over_ranks(x)` reduces a float across ranks (identity for
+    one rank).  Returns (tokens/s, ms per step)."""
+    ms = max_over_ranks(ms_local) if world > 1 else ms_local
+    return world * tokens_per_rank / (ms * 1e-3), ms
+
+
 # ------------------------------------------------------------------ our arm
 def run_ours(args, rank, world, local_rank):
     import numpy as np
@@ -226,12 +235,12 @@ def run_ours(args, rank, world, local_rank):
         t_wall = time.perf_counter() - t_wall
     barrier()
     check_status()
-    ms = ev0.elapsed_time(ev1) / args.steps
-    if dist:
-        t = torch.tensor([ms], device=dev, dtype=torch.float64)
+    def max_over_ranks(v):
+        t = torch.tensor([v], device=dev, dtype=torch.float64)
         tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-        ms = float(t.item())
-    tokens_per_s = world * T / (ms * 1e-3)
+        return float(t.item())
+
+    tokens_per_s, ms = replica_throughput(ev0.elapsed_time(ev1) / args.steps, T, world, max_over_ranks)
 
     # ---- routing kernel alone (to isolate the persistent layer kernel's time)
     ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -269,12 +278,8 @@ def run_ours(args, rank, world, local_rank):
         e2e_step()
     e1_.record(stream)
     e1_.synchronize()
-    e2e_ms = e0_.elapsed_time(e1_) / e_steps
     check_status()
-    if dist:
-        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_tps, e2e_ms = replica_throughput(e0_.elapsed_time(e1_) / e_steps, T, world, max_over_ranks)
     h2d = hx.numel() + hsf.numel() + hidx.numel() * 4 + hw.numel() * 4
     d2h = hy.numel() * 2
 
@@ -293,7 +298,7 @@ def run_ours(args, rank, world, local_rank):
                 "touched_experts": touched, "achieved_tflops": round(achieved_tflops, 1)}
     return {
         "tokens_per_s": tokens_per_s, "ms": ms, "route_ms": route_ms, "roofline": roofline,
-        "e2e": {"value": round(world * T / (e2e_ms * 1e-3), 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        "e2e": {"value": round(e2e_tps, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
         "clocks": clk.summary(), "wall_s": t_wall, "gpu_launches": 2 * args.steps,
         "cfg": cfg, "touched": touched,
