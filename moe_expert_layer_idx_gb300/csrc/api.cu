@@ -11,9 +11,12 @@
 
 namespace mm {
 __global__ void route_kernel(const RouteParams p);
-__global__ void megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant__ CUtensorMap tm_w2,
-                               const __grid_constant__ CUtensorMap tm_xs, const __grid_constant__ CUtensorMap tm_l1a,
-                               const __grid_constant__ ForwardParams p);
+int layer_smem_bytes(int variant);
+int layer_max_n(int variant);
+cudaError_t layer_prepare(int variant, int* ctas_per_sm);
+cudaError_t layer_launch(int variant, int grid, cudaStream_t stream, const CUtensorMap& tm_w1,
+                         const CUtensorMap& tm_w2, const CUtensorMap& tm_xs, const CUtensorMap& tm_l1a,
+                         const ForwardParams& p);
 cudaError_t launch_quantize(const float* src, long long nblocks, bool e4m3, uint8_t* dst, uint8_t* sf,
                             int grid, cudaStream_t stream);
 }  // namespace mm
@@ -59,8 +62,17 @@ int check_shape(long long T, int E, int k, int H, int I) {
 struct DevState {
   bool ready = false;
   int sms = 0;
-  int max_resident = 0;
+  int max_resident[kNumVariants] = {0, 0, 0};   // per kernel variant
 };
+
+// Kernel variant for a batch from its mean tokens per expert: the fewer the
+// tokens, the narrower the token tile and the deeper the ring of weight stages
+// in flight (decode batches stream weights); otherwise wide token tiles.
+int pick_variant(long long assignments, int experts) {
+  if (assignments <= 8ll * experts) return kVariantThin;
+  if (assignments <= 32ll * experts) return kVariantNarrow;
+  return kVariantWide;
+}
 std::mutex g_mu;
 DevState g_dev[128];
 
@@ -89,18 +101,19 @@ int device_state(int* dev_out, DevState** st_out) {
       }
       g_encode = reinterpret_cast<EncodeTiledFn>(fn);
     }
-    if (cudaFuncSetAttribute(megamoe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess ||
-        cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 32 * 1024 * 4) != cudaSuccess) {
+    if (cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 32 * 1024 * 4) != cudaSuccess) {
       cudaGetLastError();
       return MM_ERR_CUDA;
     }
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, megamoe_kernel, kThreads, kSmemBytes) != cudaSuccess) {
-      cudaGetLastError();
-      return MM_ERR_CUDA;
+    for (int v = 0; v < kNumVariants; ++v) {
+      int per_sm = 0;
+      if (layer_prepare(v, &per_sm) != cudaSuccess) {
+        cudaGetLastError();
+        return MM_ERR_CUDA;
+      }
+      st.max_resident[v] = per_sm * prop.multiProcessorCount;
     }
     st.sms = prop.multiProcessorCount;
-    st.max_resident = per_sm * prop.multiProcessorCount;
     st.ready = true;
   }
   *dev_out = dev;
@@ -123,6 +136,7 @@ int encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t
 int launch_route(int T, int E, int k, const int32_t* topk_idx, uint8_t* ws, const Layout& L, cudaStream_t st) {
   RouteParams rp;
   rp.T = T; rp.E = E; rp.k = k; rp.A = T * k;
+  rp.max_n = layer_max_n(pick_variant((long long)T * k, E));
   rp.topk_idx = topk_idx;
   rp.ws = ws;
   rp.L = L;
@@ -197,7 +211,8 @@ int mm_forward(int num_tokens, int experts, int topk, int hidden, int inter,
   DevState* st;
   rc = device_state(&dev, &st);
   if (rc != MM_OK) return rc;
-  const int grid = mm_grid_size(st->sms, reserved_now(), num_sms, st->max_resident);
+  const int variant = pick_variant((long long)T * k, E);
+  const int grid = mm_grid_size(st->sms, reserved_now(), num_sms, st->max_resident[variant]);
   const int A = T * k;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
 
@@ -205,7 +220,7 @@ int mm_forward(int num_tokens, int experts, int topk, int hidden, int inter,
   if (encode_2d(&tm_w1, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, l1_w, (uint64_t)H, (uint64_t)E * 2 * I, H / 2,
                 kBlockK, kL1Feat) != MM_OK ||
       encode_2d(&tm_w2, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, l2_w, (uint64_t)I, (uint64_t)E * H, I / 2,
-                kBlockK, kL2Rows) != MM_OK ||
+                kBlockK, kL2Rows / 2) != MM_OK ||
       encode_2d(&tm_xs, CU_TENSOR_MAP_DATA_TYPE_UINT8, ws + L.xs, (uint64_t)H, (uint64_t)A, H, kBlockK, 16) != MM_OK ||
       encode_2d(&tm_l1a, CU_TENSOR_MAP_DATA_TYPE_UINT8, ws + L.l1a, (uint64_t)I, (uint64_t)A, I, kBlockK, 16) != MM_OK)
     return MM_ERR_CUDA;
@@ -230,8 +245,7 @@ int mm_forward(int num_tokens, int experts, int topk, int hidden, int inter,
   fp.y = static_cast<uint16_t*>(y);
   fp.ws = ws;
   fp.L = L;
-  megamoe_kernel<<<grid, kThreads, kSmemBytes, s>>>(tm_w1, tm_w2, tm_xs, tm_l1a, fp);
-  if (cudaGetLastError() != cudaSuccess) return MM_ERR_CUDA;
+  if (layer_launch(variant, grid, s, tm_w1, tm_w2, tm_xs, tm_l1a, fp) != cudaSuccess) return MM_ERR_CUDA;
   return MM_OK;
 }
 

@@ -15,19 +15,16 @@ constexpr int kBlockK = 128;        // K per pipeline stage: 4 UE8M0 scale block
 constexpr int kL1Feat = 64;         // intermediate features per L1 tile (64 gate + 64 up rows)
 constexpr int kL2Rows = 128;        // hidden rows per L2 tile
 constexpr int kTileM = 128;         // MMA M (weight rows)
-constexpr int kMaxTileN = 240;      // tokens per tile (MMA N), multiple of 16
-constexpr int kStages = 4;          // smem pipeline depth
 constexpr int kThreads = 256;       // 8 warps per CTA
 
 constexpr int kABytes = kTileM * kBlockK;           // 16 KB: 128 rows x 128 padded FP4 bytes
 // A packed-FP4 TMA box counts its global (packed) bytes toward the barrier's
 // transaction count, not its padded shared-memory footprint.
 constexpr int kATxBytes = kTileM * kBlockK / 2;     // 8 KB per stage
-constexpr int kBBytes = kMaxTileN * kBlockK;        // 30 KB: 240 token rows x 128 B
 constexpr int kSFABytes = 512;                      // one 128-row scale atom
-constexpr int kSFBBytes = 1024;                     // two 128-row scale atoms
-constexpr int kStageBytes = kABytes + kBBytes + kSFABytes + kSFBBytes;
-static_assert(kABytes % 1024 == 0 && kBBytes % 1024 == 0, "SW128 tiles need 1 KB alignment");
+constexpr int kBarBytes = 512;                      // mbarriers + small shared state
+// Epilogue exchange buffer (two warp pairs x two directions x 8 columns x 32 lanes).
+constexpr int kXchgBytes = 2 * 2 * 8 * 32 * 4;
 
 // TMEM columns: two accumulator buffers and the scale factors of one stage.
 constexpr uint32_t kTmemCols = 512;
@@ -35,10 +32,27 @@ constexpr uint32_t kAccStride = 256;                // buffer b starts at column
 constexpr uint32_t kSFACol = 496;                   // 4 columns
 constexpr uint32_t kSFBCol = 500;                   // 8 columns
 
-// Epilogue exchange buffer (two warp pairs x two directions x 8 columns x 32 lanes).
-constexpr int kXchgBytes = 2 * 2 * 8 * 32 * 4;
-
-constexpr int kSmemBytes = kStages * kStageBytes + 256 /*barriers*/ + kXchgBytes + 1024 /*align*/;
+// A kernel variant: the largest MMA N (tokens per tile) and the depth of the
+// shared-memory ring.  Few tokens per expert (decode) leave the token tile
+// nearly empty, so that variant trades token capacity for more stages of
+// weights in flight; many tokens per expert (prefill) want wide tiles.
+template <int kMaxN_, int kStages_>
+struct Variant {
+  static constexpr int kMaxN = kMaxN_;
+  static constexpr int kStages = kStages_;
+  static constexpr int kBBytes = kMaxN * kBlockK;
+  static constexpr int kSFBBytes = kMaxN > 128 ? 1024 : 512;
+  static constexpr int kStageBytes = kABytes + kBBytes + kSFABytes + kSFBBytes;
+  static constexpr int kSmemBytes = kStages * kStageBytes + kBarBytes + kXchgBytes + 1024 /*align*/;
+  static_assert(kMaxN % 16 == 0 && kMaxN <= 240, "MMA N: multiple of 16, two accumulators fit TMEM");
+  static_assert(kBBytes % 1024 == 0, "SW128 tiles need 1 KB alignment");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+  static_assert(2 * kStages * 8 + 5 * 8 + 32 + 32 <= kBarBytes, "barrier region");
+};
+using WideVariant = Variant<240, 4>;
+using NarrowVariant = Variant<64, 8>;
+using ThinVariant = Variant<32, 10>;
+enum VariantId : int { kVariantWide = 0, kVariantNarrow = 1, kVariantThin = 2, kNumVariants = 3 };
 
 // ----------------------------------------------------------------- control block
 // 32-bit words at the head of the workspace.
@@ -81,9 +95,9 @@ __host__ __device__ inline Layout make_layout(long long T, int E, int k, int H, 
   return L;
 }
 
-// Number of tiles (MMA N blocks) an expert with `count` assignments splits into,
-// and the rows of block `b`: blocks are balanced, each at most kMaxTileN rows.
-__host__ __device__ inline int n_blocks(int count) { return (count + kMaxTileN - 1) / kMaxTileN; }
+// Number of N blocks an expert with `count` assignments splits into; blocks are
+// balanced, each at most `max_n` rows.
+__host__ __device__ inline int n_blocks(int count, int max_n) { return (count + max_n - 1) / max_n; }
 
 // ----------------------------------------------------------------- parameters
 struct ForwardParams {
@@ -108,6 +122,7 @@ struct ForwardParams {
 struct RouteParams {
   int T, E, k;
   int A;
+  int max_n;                   // largest N block of the layer kernel variant
   const int32_t* topk_idx;
   uint8_t* ws;
   Layout L;
@@ -207,6 +222,19 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_
   return true;
 }
 
+// Bounded wait used while tearing down after an abort: it ignores the abort
+// flag (the copies and MMAs in flight must land before the CTA exits) and
+// stops only at the time limit.  Returns false on timeout.
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, unsigned long long timeout_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  uint32_t it = 0;
+  while (!mbar_try_wait(bar, parity)) {
+    if ((++it & 63u) == 0u && globaltimer() - t0 > timeout_ns) return false;
+  }
+  return true;
+}
+
 // Bounded wait until a global counter reaches `target` (acquire).
 __device__ __forceinline__ bool counter_wait(const uint32_t* p, uint32_t target, uint32_t* ctrl,
                                              unsigned long long timeout_ns, uint32_t site) {
@@ -275,6 +303,14 @@ __device__ __forceinline__ void tc_mma_mx(uint32_t d_tmem, uint64_t a_desc, uint
       "setp.ne.b32 p, %6, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
       :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+// Same, always accumulating into D.
+__device__ __forceinline__ void tc_mma_mx_acc(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                              uint32_t sfa_tmem, uint32_t sfb_tmem) {
+  asm volatile(
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], 1;"
+      :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem)
       : "memory");
 }
 // 32 lanes x 16 columns of 32-bit accumulators into registers.

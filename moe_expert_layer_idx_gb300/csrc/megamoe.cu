@@ -93,10 +93,15 @@ __device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" :: "r"(bar) : "memory");
 }
 
+template <class V>
 __global__ void __launch_bounds__(kThreads, 1)
 megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant__ CUtensorMap tm_w2,
                const __grid_constant__ CUtensorMap tm_xs, const __grid_constant__ CUtensorMap tm_l1a,
                const __grid_constant__ ForwardParams p) {
+  constexpr int kStages = V::kStages;
+  constexpr int kBBytes = V::kBBytes;
+  constexpr int kSFBBytes = V::kSFBBytes;
+  constexpr int kStageBytes = V::kStageBytes;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = sm;
@@ -104,15 +109,16 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
   uint8_t* sSFA = sB + kStages * kBBytes;
   uint8_t* sSFB = sSFA + kStages * kSFABytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sSFB + kStages * kSFBBytes);
-  uint64_t* full_tma = bars;                 // [kStages] TMA bytes landed
-  uint64_t* full_sf = bars + kStages;        // [kStages] 32 scale-loader lanes' cp.async landed
-  uint64_t* empty = bars + 2 * kStages;      // [kStages] MMAs reading the stage are done
-  uint64_t* tfull = bars + 3 * kStages;      // [2] accumulator ready
+  uint64_t* full = bars;                     // [kStages] TMA bytes + 32 scale-loader lanes' cp.async landed
+  uint64_t* empty = bars + kStages;          // [kStages] MMAs reading the stage are done
+  uint64_t* tfull = bars + 2 * kStages;      // [2] accumulator ready
   uint64_t* tempty = tfull + 2;              // [2] accumulator drained (4 epilogue warps)
   uint64_t* drain = tempty + 2;              // [1] final MMA drain
-  uint32_t* s_misc = reinterpret_cast<uint32_t*>(drain + 1);   // tmem base, consumed, issued, combine-off
-  int32_t* s_vote = reinterpret_cast<int32_t*>(s_misc + 4);    // epilogue votes [2][4]
-  float* xchg = reinterpret_cast<float*>(sm + kStages * kStageBytes + 256);
+  // tmem base, stages consumed (MMA), stages issued (producer 0), combine off, stages armed (scale
+  // loader), stages issued (producer 1)
+  uint32_t* s_misc = reinterpret_cast<uint32_t*>(drain + 1);
+  int32_t* s_vote = reinterpret_cast<int32_t*>(s_misc + 8);    // epilogue votes [2][4]
+  float* xchg = reinterpret_cast<float*>(sm + kStages * kStageBytes + kBarBytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint32_t* ctrl = reinterpret_cast<uint32_t*>(p.ws + p.L.ctrl);
@@ -133,8 +139,7 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full_tma[s], 1);
-      mbar_init(&full_sf[s], 32);
+      mbar_init(&full[s], 2 + 32);
       mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -142,7 +147,7 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
       mbar_init(&tempty[b], 4);
     }
     mbar_init(drain, 1);
-    s_misc[1] = 0; s_misc[2] = 0; s_misc[3] = 0;
+    s_misc[1] = 0; s_misc[2] = 0; s_misc[3] = 0; s_misc[4] = 0; s_misc[5] = 0;
     fence_mbar_init();
     prefetch_tensormap(&tm_w1);
     prefetch_tensormap(&tm_w2);
@@ -185,9 +190,14 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
   const int total = nL1 + nItems * p.mt2;
 
   // ------------------------------------------------------------ 1. tiles
-  if (warp == 0) {
+  if (warp == 0 || warp == 3) {
     if (lane == 0) {
-      // ---------------- TMA producer
+      // ---------------- TMA producers
+      // One thread issues the TMA work of a stage at a limited rate, so two
+      // threads (warps 0 and 3) share it: producer `pid` loads weight rows
+      // [64*pid, 64*pid + 64) of the tile and the token boxes j with
+      // j % 2 == pid, arming the stage's barrier with its own bytes.
+      const int pid = warp == 0 ? 0 : 1;
       uint32_t stage = 0, phase = 0, issued = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
@@ -200,35 +210,41 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
           ok = counter_wait(&l1_done[ti.e], l1_tiles_of(items, ti.e, p.mt1), ctrl, to, (kSiteL1Done << 24) | tag);
         if (!ok) break;
         fence_proxy_async_global();
-        const uint32_t bytes = (uint32_t)(kATxBytes + ti.n * kBlockK);
+        const int nbox = ti.n / 16;
+        const int my_boxes = (nbox + 1 - pid) / 2;
+        const uint32_t bytes = (uint32_t)(kATxBytes / 2 + my_boxes * 16 * kBlockK);
+        const CUtensorMap* tm_a = ti.layer == 1 ? &tm_w1 : &tm_w2;
+        const CUtensorMap* tm_b = ti.layer == 1 ? &tm_xs : &tm_l1a;
+        // weight row of this producer's 64-row half: L1 gate rows or up rows; L2 top or bottom half
+        const int a_row = ti.layer == 1 ? ti.e * 2 * p.I + ti.mt * kL1Feat + pid * p.I
+                                        : ti.e * p.H + ti.mt * kL2Rows + pid * 64;
         for (int kb = 0; kb < ti.ks; ++kb) {
           if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, ctrl, to, (kSiteEmpty << 24) | tag)) { ok = false; break; }
-          const uint32_t fb = smem_u32(&full_tma[stage]);
+          const uint32_t fb = smem_u32(&full[stage]);
           mbar_arrive_expect_tx(fb, bytes);
-          const uint32_t a_dst = smem_u32(sA + stage * kABytes);
+          const uint32_t a_dst = smem_u32(sA + stage * kABytes) + (uint32_t)(pid * 64 * kBlockK);
           const uint32_t b_dst = smem_u32(sB + stage * kBBytes);
           const int kx = kb * kBlockK;
-          if (ti.layer == 1) {
-            const int row = ti.e * 2 * p.I + ti.mt * kL1Feat;
-            tma_load_2d(a_dst, &tm_w1, fb, kx, row);                             // gate rows
-            tma_load_2d(a_dst + kL1Feat * kBlockK, &tm_w1, fb, kx, row + p.I);   // up rows
-            for (int j = 0; j < ti.n / 16; ++j)
-              tma_load_2d(b_dst + j * 16 * kBlockK, &tm_xs, fb, kx, ti.r0 + 16 * j);
-          } else {
-            const int row = ti.e * p.H + ti.mt * kL2Rows;
-            tma_load_2d(a_dst, &tm_w2, fb, kx, row);
-            for (int j = 0; j < ti.n / 16; ++j)
-              tma_load_2d(b_dst + j * 16 * kBlockK, &tm_l1a, fb, kx, ti.r0 + 16 * j);
-          }
+          tma_load_2d(a_dst, tm_a, fb, kx, a_row);
+          for (int j = pid; j < nbox; j += 2)
+            tma_load_2d(b_dst + j * 16 * kBlockK, tm_b, fb, kx, ti.r0 + 16 * j);
           ++issued;
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
       }
-      s_misc[2] = issued;
+      s_misc[2 + 3 * pid] = issued;     // s_misc[2] (producer 0), s_misc[5] (producer 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- MMA issuer
+      // Stage s's descriptors are stage 0's plus s * (stage bytes / 16) in the
+      // start-address field (shared addresses stay below 256 KB: no carry).
+      const uint64_t a_desc0 = desc_sw128(smem_u32(sA));
+      const uint64_t b_desc0 = desc_sw128(smem_u32(sB));
+      const uint64_t sfa_desc0 = desc_sf(smem_u32(sSFA));
+      const uint64_t sfb_desc0 = desc_sf(smem_u32(sSFB));
+      const uint32_t full0 = smem_u32(&full[0]), empty0 = smem_u32(&empty[0]);
+      const uint32_t sfa_t = tmem + kSFACol, sfb_t = tmem + kSFBCol;
       uint32_t stage = 0, phase = 0, ab = 0, aphase = 0, consumed = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
@@ -238,24 +254,28 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
         if (!mbar_wait(smem_u32(&tempty[ab]), aphase ^ 1u, ctrl, to, (kSiteTmemEmpty << 24) | tag)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem + ab * kAccStride;
+        const uint32_t id0 = idesc_mx((uint32_t)ti.n, 0u);
+        const uint32_t id1 = id0 | (1u << 4) | (1u << 29);
+        const uint32_t id2 = id0 | (2u << 4) | (2u << 29);
+        const uint32_t id3 = id0 | (3u << 4) | (3u << 29);
+        const bool two_sfb = ti.n > 128;
         for (int kb = 0; kb < ti.ks; ++kb) {
-          if (!mbar_wait(smem_u32(&full_tma[stage]), phase, ctrl, to, (kSiteFull << 24) | tag) ||
-              !mbar_wait(smem_u32(&full_sf[stage]), phase, ctrl, to, (kSiteFullSf << 24) | tag)) { ok = false; break; }
+          if (!mbar_wait(full0 + stage * 8u, phase, ctrl, to, (kSiteFull << 24) | tag)) { ok = false; break; }
           tc_fence_after();
           fence_proxy_async_shared();   // scale atoms were written through the generic proxy
-          const uint32_t sfa = smem_u32(sSFA + stage * kSFABytes);
-          const uint32_t sfb = smem_u32(sSFB + stage * kSFBBytes);
-          tc_cp_sf(tmem + kSFACol, desc_sf(sfa));
-          tc_cp_sf(tmem + kSFBCol, desc_sf(sfb));
-          if (ti.n > 128) tc_cp_sf(tmem + kSFBCol + 4, desc_sf(sfb + 512));
-          const uint32_t a0 = smem_u32(sA + stage * kABytes);
-          const uint32_t b0 = smem_u32(sB + stage * kBBytes);
-#pragma unroll
-          for (int kk = 0; kk < kBlockK / 32; ++kk) {
-            tc_mma_mx(d_tmem, desc_sw128(a0 + kk * 32), desc_sw128(b0 + kk * 32), idesc_mx((uint32_t)ti.n, (uint32_t)kk),
-                      tmem + kSFACol, tmem + kSFBCol, (kb | kk) != 0 ? 1u : 0u);
-          }
-          tc_commit(smem_u32(&empty[stage]));
+          // stage offsets in 16-byte units fit the 14-bit address field of the low word
+          const uint32_t so = stage;
+          const uint64_t sfb_d = sfb_desc0 + (uint64_t)(so * (uint32_t)(kSFBBytes >> 4));
+          tc_cp_sf(sfa_t, sfa_desc0 + (uint64_t)(so * (uint32_t)(kSFABytes >> 4)));
+          tc_cp_sf(sfb_t, sfb_d);
+          if (two_sfb) tc_cp_sf(sfb_t + 4, sfb_d + (512 >> 4));
+          const uint64_t ad = a_desc0 + (uint64_t)(so * (uint32_t)(kABytes >> 4));
+          const uint64_t bd = b_desc0 + (uint64_t)(so * (uint32_t)(kBBytes >> 4));
+          tc_mma_mx(d_tmem, ad, bd, id0, sfa_t, sfb_t, kb != 0 ? 1u : 0u);
+          tc_mma_mx_acc(d_tmem, ad + 2, bd + 2, id1, sfa_t, sfb_t);     // +32 bytes along K
+          tc_mma_mx_acc(d_tmem, ad + 4, bd + 4, id2, sfa_t, sfb_t);
+          tc_mma_mx_acc(d_tmem, ad + 6, bd + 6, id3, sfa_t, sfb_t);
+          tc_commit(empty0 + stage * 8u);
           ++consumed;
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
@@ -266,11 +286,11 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
       }
       s_misc[1] = consumed;
       tc_commit(smem_u32(drain));
-      mbar_wait(smem_u32(drain), 0, ctrl, to, kSiteDrain << 24);
+      if (!mbar_wait_drain(smem_u32(drain), 0, to)) set_error(ctrl, MM_ERR_TIMEOUT, kSiteDrain << 24);
     }
   } else if (warp == 2) {
     // ---------------- scale loader (32 lanes)
-    uint32_t stage = 0, phase = 0;
+    uint32_t stage = 0, phase = 0, armed = 0;
     const int H32 = p.H / 32, I32 = p.I / 32;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       Tile ti;
@@ -324,12 +344,14 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
             }
           }
         }
-        cp_async_mbar_arrive_noinc(smem_u32(&full_sf[stage]));
+        cp_async_mbar_arrive_noinc(smem_u32(&full[stage]));
+        ++armed;
         if (++stage == kStages) { stage = 0; phase ^= 1u; }
       }
       if (!ok) break;
     }
     cp_async_wait<0>();
+    if (lane == 0) s_misc[4] = armed;
   } else if (warp >= 4) {
     // ---------------- epilogue (warps 4..7 own TMEM lanes 32q .. 32q+31)
     const int q = warp - 4;
@@ -391,7 +413,7 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
               gg = fminf(gg, L);
               uu = fminf(fmaxf(uu, -L), L);
             }
-            const float h = gg / (1.0f + __expf(-gg)) * uu;
+            const float h = gg * __fdividef(1.0f, 1.0f + __expf(-gg)) * uu;   // fast-math SiLU
             float a = fabsf(h);
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
@@ -443,10 +465,19 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
   // ------------------------------------------------------------ teardown
   __syncthreads();
   if (threadIdx.x == 0) {
-    // after an abort, TMA loads may still be landing: wait for each issued stage
-    const uint32_t issued = s_misc[2], consumed = s_misc[1];
-    for (uint32_t s = consumed; s < issued; ++s)
-      mbar_wait(smem_u32(&full_tma[s % kStages]), (s / kStages) & 1u, ctrl, to, kSiteDrain << 24);
+    // After an abort, TMA loads may still be landing.  Each issued but
+    // unconsumed stage's barrier completes once its bytes land, provided the
+    // 32 scale-loader arrivals were made; make the missing ones here.
+    const uint32_t issued0 = s_misc[2], issued1 = s_misc[5], consumed = s_misc[1], armed = s_misc[4];
+    const uint32_t issued = issued0 > issued1 ? issued0 : issued1;
+    for (uint32_t s = consumed; s < issued; ++s) {
+      const uint32_t bar = smem_u32(&full[s % kStages]);
+      if (s >= armed)
+        for (int i = 0; i < 32; ++i) mbar_arrive(bar);
+      if (s >= issued0) mbar_arrive(bar);      // a producer that stopped early: its arrival, no bytes
+      if (s >= issued1) mbar_arrive(bar);
+      if (!mbar_wait_drain(bar, (s / kStages) & 1u, to)) set_error(ctrl, MM_ERR_TIMEOUT, kSiteDrain << 24);
+    }
   }
   if (warp == 1) {
     tc_fence_after();
@@ -466,14 +497,21 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
   __syncthreads();
   if (s_misc[3] != 0u) return;
 
+  // work item = (token, up to 1024 outputs): 128 uint4 chunks of 8 bf16, 4 per lane
   const int H = p.H, k = p.k;
   const int nchunk = H / 8;
-  for (int t = blockIdx.x * (kThreads / 32) + warp; t < p.T; t += gridDim.x * (kThreads / 32)) {
+  const int per_item = 128;
+  const int items_per_token = (nchunk + per_item - 1) / per_item;
+  const int nitems = p.T * items_per_token;
+  for (int it = blockIdx.x * (kThreads / 32) + warp; it < nitems; it += gridDim.x * (kThreads / 32)) {
+    const int t = it / items_per_token;
+    const int c_beg = (it - t * items_per_token) * per_item;
+    const int c_end = min(c_beg + per_item, nchunk);
     const int idx = lane < k ? __ldg(p.topk_idx + (size_t)t * k + lane) : -1;
     const unsigned valid = __ballot_sync(0xffffffffu, idx >= 0);
     const float4* rows = reinterpret_cast<const float4*>(stage_out + (size_t)t * k * H);
     uint4* yrow = reinterpret_cast<uint4*>(p.y + (size_t)t * H);
-    for (int c = lane; c < nchunk; c += 32) {
+    for (int c = c_beg + lane; c < c_end; c += 32) {
       float acc[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) acc[i] = 0.f;
@@ -491,6 +529,43 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
       yrow[c] = make_uint4(o[0], o[1], o[2], o[3]);
     }
   }
+}
+
+// ---------------------------------------------------------------- host side
+// Template kernels are configured and launched in the translation unit that
+// defines them.
+int layer_smem_bytes(int variant) {
+  return variant == kVariantThin ? ThinVariant::kSmemBytes
+       : variant == kVariantNarrow ? NarrowVariant::kSmemBytes : WideVariant::kSmemBytes;
+}
+
+int layer_max_n(int variant) {
+  return variant == kVariantThin ? ThinVariant::kMaxN
+       : variant == kVariantNarrow ? NarrowVariant::kMaxN : WideVariant::kMaxN;
+}
+
+cudaError_t layer_prepare(int variant, int* ctas_per_sm) {
+  const void* fn = variant == kVariantThin ? (const void*)megamoe_kernel<ThinVariant>
+                 : variant == kVariantNarrow ? (const void*)megamoe_kernel<NarrowVariant>
+                                             : (const void*)megamoe_kernel<WideVariant>;
+  const int smem = layer_smem_bytes(variant);
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, fn, kThreads, smem);
+}
+
+cudaError_t layer_launch(int variant, int grid, cudaStream_t stream, const CUtensorMap& tm_w1,
+                         const CUtensorMap& tm_w2, const CUtensorMap& tm_xs, const CUtensorMap& tm_l1a,
+                         const ForwardParams& p) {
+  if (variant == kVariantThin)
+    megamoe_kernel<ThinVariant><<<grid, kThreads, ThinVariant::kSmemBytes, stream>>>(tm_w1, tm_w2, tm_xs, tm_l1a, p);
+  else if (variant == kVariantNarrow)
+    megamoe_kernel<NarrowVariant><<<grid, kThreads, NarrowVariant::kSmemBytes, stream>>>(tm_w1, tm_w2, tm_xs,
+                                                                                         tm_l1a, p);
+  else
+    megamoe_kernel<WideVariant><<<grid, kThreads, WideVariant::kSmemBytes, stream>>>(tm_w1, tm_w2, tm_xs,
+                                                                                     tm_l1a, p);
+  return cudaGetLastError();
 }
 
 }  // namespace mm

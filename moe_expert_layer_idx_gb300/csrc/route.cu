@@ -104,7 +104,7 @@ __global__ void __launch_bounds__(1024, 1) route_kernel(const RouteParams p) {
     }
   }
   const int off = block_exclusive_scan_1024(cnt, s_warp);
-  const int nb = n_blocks(cnt);
+  const int nb = n_blocks(cnt, p.max_n);
   const int nb_off = block_exclusive_scan_1024(nb, s_warp);
   if (tid < E) {
     counts[tid] = cnt;

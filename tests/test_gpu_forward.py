@@ -22,6 +22,9 @@ SMALL = {
     "sparse": synth.Config("sparse", T=37, H=256, I=128, E=16, k=4, clamp=0.0, seed=2),
     # skewed routing, wider hidden, I/64 = 6 L1 tiles per expert
     "wide": synth.Config("wide", T=129, H=1024, I=384, E=96, k=8, clamp=10.0, skew=True, seed=3),
+    # ~6 tokens per expert (the deep-ring variant for decode-sized batches), and a
+    # hot expert split into several N blocks
+    "thin": synth.Config("thin", T=100, H=512, I=256, E=64, k=4, clamp=7.0, skew=True, seed=5),
 }
 
 
