@@ -47,7 +47,7 @@ struct Variant {
   static_assert(kMaxN % 16 == 0 && kMaxN <= 240, "MMA N: multiple of 16, two accumulators fit TMEM");
   static_assert(kBBytes % 1024 == 0, "SW128 tiles need 1 KB alignment");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
-  static_assert(2 * kStages * 8 + 5 * 8 + 32 + 32 <= kBarBytes, "barrier region");
+  static_assert(2 * kStages * 8 + 5 * 8 + 2 * 4 * 8 + 32 + 32 + 16 <= kBarBytes, "barrier region");
 };
 using WideVariant = Variant<240, 4>;
 using NarrowVariant = Variant<64, 8>;
@@ -57,13 +57,18 @@ enum VariantId : int { kVariantWide = 0, kVariantNarrow = 1, kVariantThin = 2, k
 // ----------------------------------------------------------------- control block
 // 32-bit words at the head of the workspace.
 enum CtrlWord : int {
-  kStatus = 0, kErrSm = 1, kErrInfo = 2, kAbort = 3, kGridBar = 4, kSiteMask = 5, kCtrlWords = 64
+  kStatus = 0, kErrSm = 1, kErrInfo = 2, kAbort = 3, kGridBar = 4, kSiteMask = 5, kNextTile = 6, kCtrlWords = 64
 };
+
+// Tile-index ring of the dynamic schedule: depth, and the number of roles that
+// read each entry (producer 1, scale loader, MMA issuer, four epilogue warps).
+constexpr int kTileRing = 4;
+constexpr int kTileReaders = 1 + 1 + 1 + 4;
 
 // Wait sites recorded in the error info word (site << 24 | tile & 0xFFFFFF).
 enum WaitSite : uint32_t {
   kSiteFull = 1, kSiteEmpty = 2, kSiteTmemFull = 3, kSiteTmemEmpty = 4,
-  kSiteArrival = 5, kSiteL1Done = 6, kSiteGridBar = 7, kSiteDrain = 8, kSiteFullSf = 9
+  kSiteArrival = 5, kSiteL1Done = 6, kSiteGridBar = 7, kSiteDrain = 8, kSiteFullSf = 9, kSiteTileRing = 10
 };
 
 // ----------------------------------------------------------------- workspace

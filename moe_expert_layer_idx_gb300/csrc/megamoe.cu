@@ -81,6 +81,39 @@ __device__ __forceinline__ void decode_tile(int t, int nL1, const ForwardParams&
   ti.ks = l1 ? p.ks1 : p.ks2;
 }
 
+// Dynamic tile schedule.  Producer 0 claims the next tile index from a global
+// counter (reset by the routing kernel of the same launch) and publishes it in
+// a small shared-memory ring; every other role takes the indices from the ring
+// in the same order.  A negative index ends the stream.  Tiles are claimed in
+// increasing index order (all L1 tiles before any L2 tile, expert-major), so an
+// L2 tile only waits for L1 tiles that running CTAs have already claimed.
+struct TileFeed {
+  int32_t* ring;
+  uint64_t* full;
+  uint64_t* empty;
+  uint32_t i = 0;
+  __device__ TileFeed(int32_t* r, uint64_t* f, uint64_t* e) : ring(r), full(f), empty(e) {}
+
+  __device__ int claim(uint32_t* counter, int total, uint32_t* ctrl, unsigned long long to, bool& ok) {
+    const uint32_t slot = i % kTileRing, ph = (i / kTileRing) & 1u;
+    ++i;
+    if (!mbar_wait(smem_u32(&empty[slot]), ph ^ 1u, ctrl, to, kSiteTileRing << 24)) { ok = false; return -1; }
+    const int t = (int)atomicAdd(counter, 1u);
+    const int v = t < total ? t : -1;
+    ring[slot] = v;
+    mbar_arrive(smem_u32(&full[slot]));          // release: the index is visible to the readers
+    return v;
+  }
+  __device__ int take(uint32_t* ctrl, unsigned long long to, bool& ok) {
+    const uint32_t slot = i % kTileRing, ph = (i / kTileRing) & 1u;
+    ++i;
+    if (!mbar_wait(smem_u32(&full[slot]), ph, ctrl, to, kSiteTileRing << 24)) { ok = false; return -1; }
+    const int v = ring[slot];
+    mbar_arrive(smem_u32(&empty[slot]));
+    return v;
+  }
+};
+
 __device__ __forceinline__ uint32_t l1_tiles_of(const int32_t* items, int e, int mt1) {
   return (uint32_t)((__ldg(items + e + 1) - __ldg(items + e)) * mt1);
 }
@@ -114,10 +147,13 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
   uint64_t* tfull = bars + 2 * kStages;      // [2] accumulator ready
   uint64_t* tempty = tfull + 2;              // [2] accumulator drained (4 epilogue warps)
   uint64_t* drain = tempty + 2;              // [1] final MMA drain
+  uint64_t* tile_full = drain + 1;           // [kTileRing] tile index published
+  uint64_t* tile_empty = tile_full + kTileRing;   // [kTileRing] read by every consumer role
   // tmem base, stages consumed (MMA), stages issued (producer 0), combine off, stages armed (scale
   // loader), stages issued (producer 1)
-  uint32_t* s_misc = reinterpret_cast<uint32_t*>(drain + 1);
+  uint32_t* s_misc = reinterpret_cast<uint32_t*>(tile_empty + kTileRing);
   int32_t* s_vote = reinterpret_cast<int32_t*>(s_misc + 8);    // epilogue votes [2][4]
+  int32_t* s_tiles = s_vote + 8;                               // [kTileRing] claimed tile indices
   float* xchg = reinterpret_cast<float*>(sm + kStages * kStageBytes + kBarBytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -147,6 +183,10 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
       mbar_init(&tempty[b], 4);
     }
     mbar_init(drain, 1);
+    for (int i = 0; i < kTileRing; ++i) {
+      mbar_init(&tile_full[i], 1);
+      mbar_init(&tile_empty[i], kTileReaders);
+    }
     s_misc[1] = 0; s_misc[2] = 0; s_misc[3] = 0; s_misc[4] = 0; s_misc[5] = 0;
     fence_mbar_init();
     prefetch_tensormap(&tm_w1);
@@ -200,7 +240,11 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
       const int pid = warp == 0 ? 0 : 1;
       uint32_t stage = 0, phase = 0, issued = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      TileFeed feed(s_tiles, tile_full, tile_empty);
+      while (ok) {
+        const int t = pid == 0 ? feed.claim(&ctrl[kNextTile], total, ctrl, to, ok)
+                               : feed.take(ctrl, to, ok);
+        if (t < 0) break;
         Tile ti;
         decode_tile(t, nL1, p, items, counts, offsets, ti);
         const uint32_t tag = (uint32_t)t & 0xFFFFFFu;
@@ -247,7 +291,10 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
       const uint32_t sfa_t = tmem + kSFACol, sfb_t = tmem + kSFBCol;
       uint32_t stage = 0, phase = 0, ab = 0, aphase = 0, consumed = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      TileFeed feed(s_tiles, tile_full, tile_empty);
+      while (ok) {
+        const int t = feed.take(ctrl, to, ok);
+        if (t < 0) break;
         Tile ti;
         decode_tile(t, nL1, p, items, counts, offsets, ti);
         const uint32_t tag = (uint32_t)t & 0xFFFFFFu;
@@ -292,7 +339,13 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
     // ---------------- scale loader (32 lanes)
     uint32_t stage = 0, phase = 0, armed = 0;
     const int H32 = p.H / 32, I32 = p.I / 32;
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+    TileFeed feed(s_tiles, tile_full, tile_empty);
+    for (;;) {
+      bool fed = true;
+      int t = -1;
+      if (lane == 0) t = feed.take(ctrl, to, fed);
+      t = __shfl_sync(0xffffffffu, t, 0);
+      if (t < 0) break;
       Tile ti;
       decode_tile(t, nL1, p, items, counts, offsets, ti);
       const uint32_t tag = (uint32_t)t & 0xFFFFFFu;
@@ -357,13 +410,22 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
     const int q = warp - 4;
     uint32_t ab = 0, aphase = 0;
     int vote_buf = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      Tile ti;
-      decode_tile(t, nL1, p, items, counts, offsets, ti);
-      const uint32_t tag = (uint32_t)t & 0xFFFFFFu;
+    TileFeed feed(s_tiles, tile_full, tile_empty);
+    for (;;) {
       bool ok = true;
-      if (lane == 0) ok = mbar_wait(smem_u32(&tfull[ab]), aphase, ctrl, to, (kSiteTmemFull << 24) | tag);
+      int t = -1;
+      if (lane == 0) t = feed.take(ctrl, to, ok);
+      t = __shfl_sync(0xffffffffu, t, 0);
       ok = __shfl_sync(0xffffffffu, ok, 0);
+      Tile ti;
+      const uint32_t tag = (uint32_t)(t < 0 ? 0 : t) & 0xFFFFFFu;
+      if (t >= 0) {
+        decode_tile(t, nL1, p, items, counts, offsets, ti);
+        if (lane == 0) ok = mbar_wait(smem_u32(&tfull[ab]), aphase, ctrl, to, (kSiteTmemFull << 24) | tag);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+      } else {
+        ok = false;      // end of the feed (or abort): leave together
+      }
       // the four epilogue warps decide together, so none waits alone on a named barrier
       if (lane == 0) s_vote[vote_buf * 4 + q] = ok ? 1 : 0;
       named_bar_sync(3, 128);
