@@ -11,12 +11,8 @@
 
 namespace mm {
 __global__ void route_kernel(const RouteParams p);
-int layer_smem_bytes(int variant);
-int layer_max_n(int variant);
-cudaError_t layer_prepare(int variant, int* ctas_per_sm);
-cudaError_t layer_launch(int variant, int grid, cudaStream_t stream, const CUtensorMap& tm_w1,
-                         const CUtensorMap& tm_w2, const CUtensorMap& tm_xs, const CUtensorMap& tm_l1a,
-                         const ForwardParams& p);
+cudaError_t layer_prepare(int* ctas_per_sm);
+cudaError_t layer_launch(int grid, cudaStream_t stream, const CUtensorMap* maps, const ForwardParams& p);
 cudaError_t launch_quantize(const float* src, long long nblocks, bool e4m3, uint8_t* dst, uint8_t* sf,
                             int grid, cudaStream_t stream);
 }  // namespace mm
@@ -62,17 +58,8 @@ int check_shape(long long T, int E, int k, int H, int I) {
 struct DevState {
   bool ready = false;
   int sms = 0;
-  int max_resident[kNumVariants] = {0, 0, 0};   // per kernel variant
+  int max_resident = 0;   // layer kernel CTAs resident at once
 };
-
-// Kernel variant for a batch from its mean tokens per expert: the fewer the
-// tokens, the narrower the token tile and the deeper the ring of weight stages
-// in flight (decode batches stream weights); otherwise wide token tiles.
-int pick_variant(long long assignments, int experts) {
-  if (assignments <= 8ll * experts) return kVariantThin;
-  if (assignments <= 32ll * experts) return kVariantNarrow;
-  return kVariantWide;
-}
 std::mutex g_mu;
 DevState g_dev[128];
 
@@ -105,14 +92,12 @@ int device_state(int* dev_out, DevState** st_out) {
       cudaGetLastError();
       return MM_ERR_CUDA;
     }
-    for (int v = 0; v < kNumVariants; ++v) {
-      int per_sm = 0;
-      if (layer_prepare(v, &per_sm) != cudaSuccess) {
-        cudaGetLastError();
-        return MM_ERR_CUDA;
-      }
-      st.max_resident[v] = per_sm * prop.multiProcessorCount;
+    int per_sm = 0;
+    if (layer_prepare(&per_sm) != cudaSuccess) {
+      cudaGetLastError();
+      return MM_ERR_CUDA;
     }
+    st.max_resident = per_sm * prop.multiProcessorCount;
     st.sms = prop.multiProcessorCount;
     st.ready = true;
   }
@@ -136,7 +121,7 @@ int encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t
 int launch_route(int T, int E, int k, const int32_t* topk_idx, uint8_t* ws, const Layout& L, cudaStream_t st) {
   RouteParams rp;
   rp.T = T; rp.E = E; rp.k = k; rp.A = T * k;
-  rp.max_n = layer_max_n(pick_variant((long long)T * k, E));
+  rp.max_n = kTileM;
   rp.topk_idx = topk_idx;
   rp.ws = ws;
   rp.L = L;
@@ -211,18 +196,24 @@ int mm_forward(int num_tokens, int experts, int topk, int hidden, int inter,
   DevState* st;
   rc = device_state(&dev, &st);
   if (rc != MM_OK) return rc;
-  const int variant = pick_variant((long long)T * k, E);
-  const int grid = mm_grid_size(st->sms, reserved_now(), num_sms, st->max_resident[variant]);
+  const int grid = mm_grid_size(st->sms, reserved_now(), num_sms, st->max_resident);
   const int A = T * k;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
 
-  alignas(64) CUtensorMap tm_w1, tm_w2, tm_xs, tm_l1a;
-  if (encode_2d(&tm_w1, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, l1_w, (uint64_t)H, (uint64_t)E * 2 * I, H / 2,
-                kBlockK, kL1Feat) != MM_OK ||
-      encode_2d(&tm_w2, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, l2_w, (uint64_t)I, (uint64_t)E * H, I / 2,
-                kBlockK, kL2Rows / 2) != MM_OK ||
-      encode_2d(&tm_xs, CU_TENSOR_MAP_DATA_TYPE_UINT8, ws + L.xs, (uint64_t)H, (uint64_t)A, H, kBlockK, 16) != MM_OK ||
-      encode_2d(&tm_l1a, CU_TENSOR_MAP_DATA_TYPE_UINT8, ws + L.l1a, (uint64_t)I, (uint64_t)A, I, kBlockK, 16) != MM_OK)
+  // W1 / W2 as [rows][K] packed FP4, 128 x 128 boxes (widened to 8-bit containers
+  // in shared memory); dispatched tokens and L1 activations as [A][K] bytes,
+  // 16-row and 128-row boxes.
+  alignas(64) CUtensorMap maps[6];
+  if (encode_2d(&maps[0], CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, l1_w, (uint64_t)H, (uint64_t)E * 2 * I, H / 2,
+                kBlockK, 128) != MM_OK ||
+      encode_2d(&maps[1], CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, l2_w, (uint64_t)I, (uint64_t)E * H, I / 2,
+                kBlockK, 128) != MM_OK ||
+      encode_2d(&maps[2], CU_TENSOR_MAP_DATA_TYPE_UINT8, ws + L.xs, (uint64_t)H, (uint64_t)A, H, kBlockK, 16) != MM_OK ||
+      encode_2d(&maps[3], CU_TENSOR_MAP_DATA_TYPE_UINT8, ws + L.xs, (uint64_t)H, (uint64_t)A, H, kBlockK,
+                kTileM) != MM_OK ||
+      encode_2d(&maps[4], CU_TENSOR_MAP_DATA_TYPE_UINT8, ws + L.l1a, (uint64_t)I, (uint64_t)A, I, kBlockK, 16) != MM_OK ||
+      encode_2d(&maps[5], CU_TENSOR_MAP_DATA_TYPE_UINT8, ws + L.l1a, (uint64_t)I, (uint64_t)A, I, kBlockK,
+                kTileM) != MM_OK)
     return MM_ERR_CUDA;
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -231,10 +222,11 @@ int mm_forward(int num_tokens, int experts, int topk, int hidden, int inter,
 
   ForwardParams fp;
   fp.T = T; fp.E = E; fp.k = k; fp.H = H; fp.I = I; fp.A = A;
-  fp.mt1 = I / kL1Feat; fp.mt2 = H / kL2Rows;
+  fp.mt1 = I / kL1Feat; fp.mt2 = (H + kTileN - 1) / kTileN;
   fp.ks1 = H / kBlockK; fp.ks2 = I / kBlockK;
   fp.use_clamp = (std::isfinite(clamp) && clamp > 0.f) ? 1 : 0;
   fp.clamp = fp.use_clamp ? clamp : 0.f;
+  fp.a_box128 = A >= kTileM ? 1 : 0;
   fp.timeout_ns = g_timeout_ns.load();
   fp.x = static_cast<const uint8_t*>(x);
   fp.x_sf = static_cast<const uint8_t*>(x_sf);
@@ -245,7 +237,7 @@ int mm_forward(int num_tokens, int experts, int topk, int hidden, int inter,
   fp.y = static_cast<uint16_t*>(y);
   fp.ws = ws;
   fp.L = L;
-  if (layer_launch(variant, grid, s, tm_w1, tm_w2, tm_xs, tm_l1a, fp) != cudaSuccess) return MM_ERR_CUDA;
+  if (layer_launch(grid, s, maps, fp) != cudaSuccess) return MM_ERR_CUDA;
   return MM_OK;
 }
 

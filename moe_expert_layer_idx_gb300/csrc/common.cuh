@@ -11,48 +11,37 @@
 namespace mm {
 
 // ----------------------------------------------------------------- geometry
+// One MMA tile: up to 128 tokens of one expert on M (E4M3, operand A) times
+// 256 weight rows on N (E2M1, operand B), K staged 128 at a time.  Putting the
+// weights on N makes every tcgen05.mma consume 4 KB of FP4 weights, so the
+// tensor pipe's per-instruction cost stays below the weight stream even when
+// an expert holds only a few tokens (decode batches).
 constexpr int kBlockK = 128;        // K per pipeline stage: 4 UE8M0 scale blocks of 32
-constexpr int kL1Feat = 64;         // intermediate features per L1 tile (64 gate + 64 up rows)
-constexpr int kL2Rows = 128;        // hidden rows per L2 tile
-constexpr int kTileM = 128;         // MMA M (weight rows)
-constexpr int kThreads = 256;       // 8 warps per CTA
+constexpr int kTileM = 128;         // MMA M: tokens per tile
+constexpr int kTileN = 256;         // MMA N: weight rows per tile
+constexpr int kL1Feat = 128;        // intermediate features per L1 tile (128 gate + 128 up rows)
+constexpr int kStages = 4;          // shared-memory ring depth
+constexpr int kEpiWarps = 8;        // epilogue warps: two per 32-lane TMEM quarter
+constexpr int kThreads = 32 * (4 + kEpiWarps);   // producer, MMA, scale loader, producer, epilogue
 
-constexpr int kABytes = kTileM * kBlockK;           // 16 KB: 128 rows x 128 padded FP4 bytes
+constexpr int kABytes = kTileM * kBlockK;           // 16 KB: 128 token rows x 128 E4M3 bytes
+constexpr int kBBytes = kTileN * kBlockK;           // 32 KB: 256 weight rows x 128 padded FP4 bytes
 // A packed-FP4 TMA box counts its global (packed) bytes toward the barrier's
 // transaction count, not its padded shared-memory footprint.
-constexpr int kATxBytes = kTileM * kBlockK / 2;     // 8 KB per stage
-constexpr int kSFABytes = 512;                      // one 128-row scale atom
+constexpr int kBHalfTxBytes = 128 * kBlockK / 2;    // 8 KB: one 128-row weight box
+constexpr int kSFABytes = 512;                      // one 128-row scale atom (tokens)
+constexpr int kSFBBytes = 1024;                     // two 128-row scale atoms (weights)
+constexpr int kStageBytes = kABytes + kBBytes + kSFABytes + kSFBBytes;
 constexpr int kBarBytes = 512;                      // mbarriers + small shared state
-// Epilogue exchange buffer (two warp pairs x two directions x 8 columns x 32 lanes).
-constexpr int kXchgBytes = 2 * 2 * 8 * 32 * 4;
+constexpr int kSmemBytes = kStages * kStageBytes + kBarBytes + 1024 /*align*/;
+static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+static_assert(kABytes % 1024 == 0 && kBBytes % 1024 == 0, "SW128 tiles need 1 KB alignment");
 
-// TMEM columns: two accumulator buffers and the scale factors of one stage.
+// TMEM columns: one 256-column fp32 accumulator, then the scale factors of the
+// stage in flight (two accumulators and the scales would need 524 columns).
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kAccStride = 256;                // buffer b starts at column 256*b
-constexpr uint32_t kSFACol = 496;                   // 4 columns
-constexpr uint32_t kSFBCol = 500;                   // 8 columns
-
-// A kernel variant: the largest MMA N (tokens per tile) and the depth of the
-// shared-memory ring.  Few tokens per expert (decode) leave the token tile
-// nearly empty, so that variant trades token capacity for more stages of
-// weights in flight; many tokens per expert (prefill) want wide tiles.
-template <int kMaxN_, int kStages_>
-struct Variant {
-  static constexpr int kMaxN = kMaxN_;
-  static constexpr int kStages = kStages_;
-  static constexpr int kBBytes = kMaxN * kBlockK;
-  static constexpr int kSFBBytes = kMaxN > 128 ? 1024 : 512;
-  static constexpr int kStageBytes = kABytes + kBBytes + kSFABytes + kSFBBytes;
-  static constexpr int kSmemBytes = kStages * kStageBytes + kBarBytes + kXchgBytes + 1024 /*align*/;
-  static_assert(kMaxN % 16 == 0 && kMaxN <= 240, "MMA N: multiple of 16, two accumulators fit TMEM");
-  static_assert(kBBytes % 1024 == 0, "SW128 tiles need 1 KB alignment");
-  static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
-  static_assert(2 * kStages * 8 + 5 * 8 + 2 * 4 * 8 + 32 + 32 + 16 <= kBarBytes, "barrier region");
-};
-using WideVariant = Variant<240, 4>;
-using NarrowVariant = Variant<64, 8>;
-using ThinVariant = Variant<32, 10>;
-enum VariantId : int { kVariantWide = 0, kVariantNarrow = 1, kVariantThin = 2, kNumVariants = 3 };
+constexpr uint32_t kSFACol = 256;                   // 4 columns
+constexpr uint32_t kSFBCol = 260;                   // 8 columns
 
 // ----------------------------------------------------------------- control block
 // 32-bit words at the head of the workspace.
@@ -61,9 +50,11 @@ enum CtrlWord : int {
 };
 
 // Tile-index ring of the dynamic schedule: depth, and the number of roles that
-// read each entry (producer 1, scale loader, MMA issuer, four epilogue warps).
+// read each entry (producer 1, scale loader, MMA issuer, the epilogue warps).
 constexpr int kTileRing = 4;
-constexpr int kTileReaders = 1 + 1 + 1 + 4;
+constexpr int kTileReaders = 1 + 1 + 1 + kEpiWarps;
+static_assert((3 * kStages + 3 + 2 * kTileRing) * 8 + 8 * 4 + 2 * kEpiWarps * 4 + kTileRing * 4 <= kBarBytes,
+              "barrier region");
 
 // Wait sites recorded in the error info word (site << 24 | tile & 0xFFFFFF).
 enum WaitSite : uint32_t {
@@ -100,18 +91,19 @@ __host__ __device__ inline Layout make_layout(long long T, int E, int k, int H, 
   return L;
 }
 
-// Number of N blocks an expert with `count` assignments splits into; blocks are
-// balanced, each at most `max_n` rows.
+// Number of token blocks an expert with `count` assignments splits into;
+// blocks are balanced, each at most `max_n` rows.
 __host__ __device__ inline int n_blocks(int count, int max_n) { return (count + max_n - 1) / max_n; }
 
 // ----------------------------------------------------------------- parameters
 struct ForwardParams {
   int T, E, k, H, I;
   int A;                       // T * k
-  int mt1, mt2;                // L1 / L2 tiles per (expert, N block): I/64, H/128
+  int mt1, mt2;                // weight blocks per expert: I/128 (L1), ceil(H/256) (L2)
   int ks1, ks2;                // K stages of L1 / L2: H/128, I/128
   int use_clamp;
   float clamp;
+  int a_box128;                // token count allows one 128-row TMA box per stage
   unsigned long long timeout_ns;
   const uint8_t* x;
   const uint8_t* x_sf;
@@ -127,7 +119,7 @@ struct ForwardParams {
 struct RouteParams {
   int T, E, k;
   int A;
-  int max_n;                   // largest N block of the layer kernel variant
+  int max_n;                   // largest token block of the layer kernel
   const int32_t* topk_idx;
   uint8_t* ws;
   Layout L;
@@ -352,14 +344,14 @@ __device__ __forceinline__ uint64_t desc_sf(uint32_t saddr) {
   d |= (uint64_t)1 << 46;
   return d;
 }
-// Instruction descriptor of kind::mxf8f6f4 with UE8M0 scales: A = E2M1 weights
-// (M = 128), B = E4M3 tokens (N), both K-major; sf_id selects the scale byte
+// Instruction descriptor of kind::mxf8f6f4 with UE8M0 scales: A = E4M3 tokens
+// (M = 128), B = E2M1 weights (N), both K-major; sf_id selects the scale byte
 // (the 32-element K block within the 128-element stage).
 __device__ __forceinline__ uint32_t idesc_mx(uint32_t n, uint32_t sf_id) {
   uint32_t d = 0;
   d |= sf_id << 4;                 // B scale-factor id
-  d |= 5u << 7;                    // A format: E2M1
-  d |= 0u << 10;                   // B format: E4M3
+  d |= 0u << 7;                    // A format: E4M3
+  d |= 5u << 10;                   // B format: E2M1
   d |= (n >> 3) << 17;             // N / 8
   d |= 1u << 23;                   // scale format: UE8M0
   d |= (128u >> 4) << 24;          // M / 16

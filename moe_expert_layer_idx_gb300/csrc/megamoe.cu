@@ -8,31 +8,35 @@
 //     scales) into the workspace and bumps that expert's arrival counter with
 //     a release -- the "token/SF pull ... l1_arrival_count release" of the
 //     DeepGEMM SM90 MegaMoE dev log (Phase 2 entry), restricted to one GPU.
-//  1. tiles, warp-specialised, statically scheduled (tile t -> CTA t % grid):
-//       warp 0 / lane 0  TMA producer: FP4 weight rows (packed -> padded 8-bit
-//                        containers by the 16U4_ALIGN16B tensor map) and FP8
-//                        token rows, 128-byte swizzled, 4-stage ring;
-//       warp 1 / lane 0  MMA issuer: scale atoms -> TMEM (tcgen05.cp), then
-//                        4 x tcgen05.mma kind::mxf8f6f4 block_scale (K = 32
-//                        each) per stage into a double-buffered TMEM
-//                        accumulator (M = 128 weight rows, N = tokens);
-//       warp 2           scale loader: gathers the UE8M0 scale bytes of the
-//                        stage into the 32x4x4 atom layout with cp.async;
-//       warps 4-7        epilogue: tcgen05.ld the accumulator.
-//     L1 tiles (expert e, 64 intermediate features, <= 240 tokens): rows
-//     [0,64) of the tile are gate rows, [64,128) up rows; the epilogue pairs
-//     them, applies the clamp and SwiGLU, requantises each 32-feature block to
-//     E4M3 + UE8M0, writes l1_acts, and releases the expert's L1-done count.
-//     L2 tiles (expert e, 128 hidden rows) wait for that count, multiply by
-//     the token's top-k weight and write fp32 rows indexed by the flat
-//     assignment (fp32, not bf16: when a token's k contributions cancel, a
-//     bf16 rounding of each one is large next to their sum).  (Weights sit on the MMA M side and tokens on N so that a
-//     decode batch with a handful of tokens per expert wastes no tensor work.)
+//  1. tiles, warp-specialised, dynamically scheduled (see TileFeed):
+//       warps 0 and 3, lane 0  TMA producers; they split each stage's boxes;
+//       warp 1, lane 0         MMA issuer: scale atoms -> TMEM (tcgen05.cp),
+//                              then 4 x tcgen05.mma kind::mxf8f6f4 block_scale
+//                              (K = 32 each) per 128-wide K stage;
+//       warp 2                 scale loader: gathers the stage's UE8M0 bytes
+//                              into the 32x4x4 atom layout with cp.async;
+//       warps 4-11             epilogue: warp w reads TMEM lanes 32(w%4)..+31,
+//                              the two warps of a lane quarter split the columns.
+//     The MMA puts up to 128 tokens of one expert on M (E4M3, operand A) and
+//     256 weight rows on N (E2M1, operand B, 128-byte swizzled, packed FP4
+//     widened to 8-bit containers by the 16U4_ALIGN16B tensor map).  Each MMA
+//     instruction consumes 4 KB of FP4 weights, which keeps the tensor pipe's
+//     per-instruction cost under the weight stream at decode batch sizes.
+//     L1 tile (expert e, 128 intermediate features, a token block): B rows
+//     [0,128) are the gate rows and [128,256) the up rows of those features, so
+//     TMEM lane m holds both halves of token m; its epilogue thread applies the
+//     clamp and SwiGLU, requantises each 32 features to E4M3 + UE8M0 in
+//     registers, writes its l1_acts row, and the tile releases the expert's
+//     L1-done count.  L2 tile (expert e, 256 hidden rows -- 128 for a tail --,
+//     a token block) waits for that count, multiplies by the token's top-k
+//     weight and writes fp32 rows indexed by the flat assignment (fp32, not
+//     bf16: when a token's k contributions cancel, a bf16 rounding of each one
+//     is large next to their sum).
 //  2. whole-grid software barrier, then the combine: y[t] = bf16(sum_j of the
 //     weighted rows t*k + j, in ascending j).
 //
 // Every wait is bounded (global timer + abort flag): a wait that runs out
-// records MM_ERR_TIMEOUT with the SM and the wait site, raises the abort flag
+// records MM_ERR_TIMEOUT with the SM and the wait site, raises the abort flag,
 // and the CTA drains its own in-flight copies and MMAs, frees its TMEM and
 // returns -- the pages' kernel reports "grid sync timeout: sm=.., thread=..,
 // grid_sync_idx=.." (digest of PR #36657, 功能与动机) instead of hanging.
@@ -46,38 +50,43 @@ namespace mm {
 struct Tile {
   int layer;   // 1 or 2
   int e;       // expert
-  int mt;      // M block: 64-feature block (L1) or 128-row block (L2)
-  int r0;      // first slot of the N block
-  int rows;    // valid tokens in the N block
-  int n;       // MMA N (rows rounded up to 16)
+  int nb;      // weight block: 128 intermediate features (L1) or 256 hidden rows (L2)
+  int r0;      // first slot of the token block
+  int rows;    // tokens in the block (<= 128)
+  int m16;     // rows rounded up to 16: token rows loaded
+  int n;       // MMA N: 256, or 128 for a hidden tail
   int ks;      // K stages
 };
 
+// Tiles are numbered L1 first, then L2; within a layer expert-major, then the
+// weight block, then the token block, so the token blocks that share a weight
+// tile run close together and find it in L2.
 __device__ __forceinline__ void decode_tile(int t, int nL1, const ForwardParams& p, const int32_t* items,
                                             const int32_t* counts, const int32_t* offsets, Tile& ti) {
   const bool l1 = t < nL1;
   const int tt = l1 ? t : t - nL1;
-  const int MT = l1 ? p.mt1 : p.mt2;
-  int lo = 0, hi = p.E;   // largest e with items[e] * MT <= tt
+  const int NB = l1 ? p.mt1 : p.mt2;
+  int lo = 0, hi = p.E;   // largest e with items[e] * NB <= tt
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
-    if (__ldg(items + mid) * MT <= tt) lo = mid; else hi = mid;
+    if (__ldg(items + mid) * NB <= tt) lo = mid; else hi = mid;
   }
   const int e = lo;
   const int i0 = __ldg(items + e);
-  const int nbk = __ldg(items + e + 1) - i0;
-  const int local = tt - i0 * MT;
-  const int mt = local / nbk;
-  const int nb = local - mt * nbk;
+  const int mbk = __ldg(items + e + 1) - i0;    // token blocks of this expert
+  const int local = tt - i0 * NB;
+  const int nb = local / mbk;
+  const int mb = local - nb * mbk;
   const int cnt = __ldg(counts + e);
-  const int rpb = (cnt + nbk - 1) / nbk;
-  const int start = nb * rpb;
+  const int rpb = (cnt + mbk - 1) / mbk;
+  const int start = mb * rpb;
   ti.layer = l1 ? 1 : 2;
   ti.e = e;
-  ti.mt = mt;
+  ti.nb = nb;
   ti.r0 = __ldg(offsets + e) + start;
   ti.rows = min(rpb, cnt - start);
-  ti.n = (ti.rows + 15) & ~15;
+  ti.m16 = (ti.rows + 15) & ~15;
+  ti.n = l1 ? kTileN : min(kTileN, p.H - nb * kTileN);
   ti.ks = l1 ? p.ks1 : p.ks2;
 }
 
@@ -126,35 +135,30 @@ __device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" :: "r"(bar) : "memory");
 }
 
-template <class V>
 __global__ void __launch_bounds__(kThreads, 1)
 megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant__ CUtensorMap tm_w2,
-               const __grid_constant__ CUtensorMap tm_xs, const __grid_constant__ CUtensorMap tm_l1a,
+               const __grid_constant__ CUtensorMap tm_xs16, const __grid_constant__ CUtensorMap tm_xs128,
+               const __grid_constant__ CUtensorMap tm_l1a16, const __grid_constant__ CUtensorMap tm_l1a128,
                const __grid_constant__ ForwardParams p) {
-  constexpr int kStages = V::kStages;
-  constexpr int kBBytes = V::kBBytes;
-  constexpr int kSFBBytes = V::kSFBBytes;
-  constexpr int kStageBytes = V::kStageBytes;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sA = sm;
-  uint8_t* sB = sA + kStages * kABytes;
-  uint8_t* sSFA = sB + kStages * kBBytes;
-  uint8_t* sSFB = sSFA + kStages * kSFABytes;
+  uint8_t* sA = sm;                                   // [kStages] token rows
+  uint8_t* sB = sA + kStages * kABytes;               // [kStages] weight rows
+  uint8_t* sSFA = sB + kStages * kBBytes;             // [kStages] token scale atom
+  uint8_t* sSFB = sSFA + kStages * kSFABytes;         // [kStages] two weight scale atoms
   uint64_t* bars = reinterpret_cast<uint64_t*>(sSFB + kStages * kSFBBytes);
   uint64_t* full = bars;                     // [kStages] TMA bytes + 32 scale-loader lanes' cp.async landed
   uint64_t* empty = bars + kStages;          // [kStages] MMAs reading the stage are done
-  uint64_t* tfull = bars + 2 * kStages;      // [2] accumulator ready
-  uint64_t* tempty = tfull + 2;              // [2] accumulator drained (4 epilogue warps)
-  uint64_t* drain = tempty + 2;              // [1] final MMA drain
+  uint64_t* tfull = bars + 2 * kStages;      // accumulator ready
+  uint64_t* tempty = tfull + 1;              // accumulator drained (every epilogue warp)
+  uint64_t* drain = tempty + 1;              // final MMA drain
   uint64_t* tile_full = drain + 1;           // [kTileRing] tile index published
   uint64_t* tile_empty = tile_full + kTileRing;   // [kTileRing] read by every consumer role
   // tmem base, stages consumed (MMA), stages issued (producer 0), combine off, stages armed (scale
   // loader), stages issued (producer 1)
   uint32_t* s_misc = reinterpret_cast<uint32_t*>(tile_empty + kTileRing);
-  int32_t* s_vote = reinterpret_cast<int32_t*>(s_misc + 8);    // epilogue votes [2][4]
-  int32_t* s_tiles = s_vote + 8;                               // [kTileRing] claimed tile indices
-  float* xchg = reinterpret_cast<float*>(sm + kStages * kStageBytes + kBarBytes);
+  int32_t* s_vote = reinterpret_cast<int32_t*>(s_misc + 8);    // epilogue votes [2][kEpiWarps]
+  int32_t* s_tiles = s_vote + 2 * kEpiWarps;                   // [kTileRing] claimed tile indices
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint32_t* ctrl = reinterpret_cast<uint32_t*>(p.ws + p.L.ctrl);
@@ -178,21 +182,21 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
       mbar_init(&full[s], 2 + 32);
       mbar_init(&empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 4);
-    }
+    mbar_init(tfull, 1);
+    mbar_init(tempty, kEpiWarps);
     mbar_init(drain, 1);
     for (int i = 0; i < kTileRing; ++i) {
       mbar_init(&tile_full[i], 1);
       mbar_init(&tile_empty[i], kTileReaders);
     }
-    s_misc[1] = 0; s_misc[2] = 0; s_misc[3] = 0; s_misc[4] = 0; s_misc[5] = 0;
+    for (int i = 1; i < 8; ++i) s_misc[i] = 0;
     fence_mbar_init();
     prefetch_tensormap(&tm_w1);
     prefetch_tensormap(&tm_w2);
-    prefetch_tensormap(&tm_xs);
-    prefetch_tensormap(&tm_l1a);
+    prefetch_tensormap(&tm_xs16);
+    prefetch_tensormap(&tm_xs128);
+    prefetch_tensormap(&tm_l1a16);
+    prefetch_tensormap(&tm_l1a128);
   }
   if (warp == 1) {
     tc_alloc(smem_u32(&s_misc[0]), kTmemCols);
@@ -233,17 +237,17 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
   if (warp == 0 || warp == 3) {
     if (lane == 0) {
       // ---------------- TMA producers
-      // One thread issues the TMA work of a stage at a limited rate, so two
-      // threads (warps 0 and 3) share it: producer `pid` loads weight rows
-      // [64*pid, 64*pid + 64) of the tile and the token boxes j with
-      // j % 2 == pid, arming the stage's barrier with its own bytes.
+      // One thread issues TMA at a limited rate, so two threads share each
+      // stage: producer `pid` loads weight rows [128*pid, 128*pid + 128) of the
+      // tile (L1: the gate rows, then the up rows) and the 16-row token boxes j
+      // with j % 2 == pid (a single 128-row token box goes to producer 0), and
+      // arms the stage's barrier with its own bytes.
       const int pid = warp == 0 ? 0 : 1;
       uint32_t stage = 0, phase = 0, issued = 0;
       bool ok = true;
       TileFeed feed(s_tiles, tile_full, tile_empty);
       while (ok) {
-        const int t = pid == 0 ? feed.claim(&ctrl[kNextTile], total, ctrl, to, ok)
-                               : feed.take(ctrl, to, ok);
+        const int t = pid == 0 ? feed.claim(&ctrl[kNextTile], total, ctrl, to, ok) : feed.take(ctrl, to, ok);
         if (t < 0) break;
         Tile ti;
         decode_tile(t, nL1, p, items, counts, offsets, ti);
@@ -254,24 +258,29 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
           ok = counter_wait(&l1_done[ti.e], l1_tiles_of(items, ti.e, p.mt1), ctrl, to, (kSiteL1Done << 24) | tag);
         if (!ok) break;
         fence_proxy_async_global();
-        const int nbox = ti.n / 16;
-        const int my_boxes = (nbox + 1 - pid) / 2;
-        const uint32_t bytes = (uint32_t)(kATxBytes / 2 + my_boxes * 16 * kBlockK);
-        const CUtensorMap* tm_a = ti.layer == 1 ? &tm_w1 : &tm_w2;
-        const CUtensorMap* tm_b = ti.layer == 1 ? &tm_xs : &tm_l1a;
-        // weight row of this producer's 64-row half: L1 gate rows or up rows; L2 top or bottom half
-        const int a_row = ti.layer == 1 ? ti.e * 2 * p.I + ti.mt * kL1Feat + pid * p.I
-                                        : ti.e * p.H + ti.mt * kL2Rows + pid * 64;
+        const bool full_box = p.a_box128 && ti.m16 == kTileM;
+        const int nbox = ti.m16 / 16;
+        const int my_a_bytes = full_box ? (pid == 0 ? kABytes : 0) : ((nbox + 1 - pid) / 2) * 16 * kBlockK;
+        const bool my_b = pid == 0 || ti.n > 128;
+        const uint32_t bytes = (uint32_t)((my_b ? kBHalfTxBytes : 0) + my_a_bytes);
+        const CUtensorMap* tm_b = ti.layer == 1 ? &tm_w1 : &tm_w2;
+        const CUtensorMap* tm_a = ti.layer == 1 ? (full_box ? &tm_xs128 : &tm_xs16)
+                                                : (full_box ? &tm_l1a128 : &tm_l1a16);
+        const int b_row = ti.layer == 1 ? ti.e * 2 * p.I + ti.nb * kL1Feat + pid * p.I
+                                        : ti.e * p.H + ti.nb * kTileN + pid * 128;
         for (int kb = 0; kb < ti.ks; ++kb) {
           if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, ctrl, to, (kSiteEmpty << 24) | tag)) { ok = false; break; }
           const uint32_t fb = smem_u32(&full[stage]);
           mbar_arrive_expect_tx(fb, bytes);
-          const uint32_t a_dst = smem_u32(sA + stage * kABytes) + (uint32_t)(pid * 64 * kBlockK);
-          const uint32_t b_dst = smem_u32(sB + stage * kBBytes);
+          const uint32_t a_dst = smem_u32(sA + stage * kABytes);
+          const uint32_t b_dst = smem_u32(sB + stage * kBBytes) + (uint32_t)(pid * 128 * kBlockK);
           const int kx = kb * kBlockK;
-          tma_load_2d(a_dst, tm_a, fb, kx, a_row);
-          for (int j = pid; j < nbox; j += 2)
-            tma_load_2d(b_dst + j * 16 * kBlockK, tm_b, fb, kx, ti.r0 + 16 * j);
+          if (my_b) tma_load_2d(b_dst, tm_b, fb, kx, b_row);
+          if (full_box) {
+            if (pid == 0) tma_load_2d(a_dst, tm_a, fb, kx, ti.r0);
+          } else {
+            for (int j = pid; j < nbox; j += 2) tma_load_2d(a_dst + j * 16 * kBlockK, tm_a, fb, kx, ti.r0 + 16 * j);
+          }
           ++issued;
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
@@ -289,7 +298,7 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
       const uint64_t sfb_desc0 = desc_sf(smem_u32(sSFB));
       const uint32_t full0 = smem_u32(&full[0]), empty0 = smem_u32(&empty[0]);
       const uint32_t sfa_t = tmem + kSFACol, sfb_t = tmem + kSFBCol;
-      uint32_t stage = 0, phase = 0, ab = 0, aphase = 0, consumed = 0;
+      uint32_t stage = 0, phase = 0, aphase = 0, consumed = 0;
       bool ok = true;
       TileFeed feed(s_tiles, tile_full, tile_empty);
       while (ok) {
@@ -298,9 +307,8 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
         Tile ti;
         decode_tile(t, nL1, p, items, counts, offsets, ti);
         const uint32_t tag = (uint32_t)t & 0xFFFFFFu;
-        if (!mbar_wait(smem_u32(&tempty[ab]), aphase ^ 1u, ctrl, to, (kSiteTmemEmpty << 24) | tag)) break;
+        if (!mbar_wait(smem_u32(tempty), aphase ^ 1u, ctrl, to, (kSiteTmemEmpty << 24) | tag)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem + ab * kAccStride;
         const uint32_t id0 = idesc_mx((uint32_t)ti.n, 0u);
         const uint32_t id1 = id0 | (1u << 4) | (1u << 29);
         const uint32_t id2 = id0 | (2u << 4) | (2u << 29);
@@ -310,7 +318,6 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
           if (!mbar_wait(full0 + stage * 8u, phase, ctrl, to, (kSiteFull << 24) | tag)) { ok = false; break; }
           tc_fence_after();
           fence_proxy_async_shared();   // scale atoms were written through the generic proxy
-          // stage offsets in 16-byte units fit the 14-bit address field of the low word
           const uint32_t so = stage;
           const uint64_t sfb_d = sfb_desc0 + (uint64_t)(so * (uint32_t)(kSFBBytes >> 4));
           tc_cp_sf(sfa_t, sfa_desc0 + (uint64_t)(so * (uint32_t)(kSFABytes >> 4)));
@@ -318,18 +325,17 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
           if (two_sfb) tc_cp_sf(sfb_t + 4, sfb_d + (512 >> 4));
           const uint64_t ad = a_desc0 + (uint64_t)(so * (uint32_t)(kABytes >> 4));
           const uint64_t bd = b_desc0 + (uint64_t)(so * (uint32_t)(kBBytes >> 4));
-          tc_mma_mx(d_tmem, ad, bd, id0, sfa_t, sfb_t, kb != 0 ? 1u : 0u);
-          tc_mma_mx_acc(d_tmem, ad + 2, bd + 2, id1, sfa_t, sfb_t);     // +32 bytes along K
-          tc_mma_mx_acc(d_tmem, ad + 4, bd + 4, id2, sfa_t, sfb_t);
-          tc_mma_mx_acc(d_tmem, ad + 6, bd + 6, id3, sfa_t, sfb_t);
+          tc_mma_mx(tmem, ad, bd, id0, sfa_t, sfb_t, kb != 0 ? 1u : 0u);
+          tc_mma_mx_acc(tmem, ad + 2, bd + 2, id1, sfa_t, sfb_t);     // +32 bytes along K
+          tc_mma_mx_acc(tmem, ad + 4, bd + 4, id2, sfa_t, sfb_t);
+          tc_mma_mx_acc(tmem, ad + 6, bd + 6, id3, sfa_t, sfb_t);
           tc_commit(empty0 + stage * 8u);
           ++consumed;
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
-        tc_commit(smem_u32(&tfull[ab]));
-        ab ^= 1u;
-        if (ab == 0) aphase ^= 1u;
+        tc_commit(smem_u32(tfull));
+        aphase ^= 1u;
       }
       s_misc[1] = consumed;
       tc_commit(smem_u32(drain));
@@ -360,19 +366,13 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
       __syncwarp();
       // every lane acquires the producers' writes before reading them
       if (ti.layer == 1) (void)ld_acquire(&arrival[ti.e]); else (void)ld_acquire(&l1_done[ti.e]);
-      const uint8_t* a_sf_base;
-      int a_stride, a_row0, a_row_up;
-      const uint8_t* b_sf_base;
-      int b_stride;
-      if (ti.layer == 1) {
-        a_sf_base = p.w1_sf; a_stride = H32;
-        a_row0 = ti.e * 2 * p.I + ti.mt * kL1Feat; a_row_up = a_row0 + p.I - kL1Feat;
-        b_sf_base = xs_sf; b_stride = H32;
-      } else {
-        a_sf_base = p.w2_sf; a_stride = I32;
-        a_row0 = ti.e * p.H + ti.mt * kL2Rows; a_row_up = a_row0;
-        b_sf_base = l1a_sf; b_stride = I32;
-      }
+      // A: the block's token rows; B: the tile's weight rows in two 128-row atoms
+      const uint8_t* a_sf_base = ti.layer == 1 ? xs_sf : l1a_sf;
+      const uint8_t* b_sf_base = ti.layer == 1 ? p.w1_sf : p.w2_sf;
+      const int kstride = ti.layer == 1 ? H32 : I32;
+      const int b_row0 = ti.layer == 1 ? ti.e * 2 * p.I + ti.nb * kL1Feat : ti.e * p.H + ti.nb * kTileN;
+      const int b_row1 = ti.layer == 1 ? b_row0 + p.I : b_row0 + 128;
+      const bool two_sfb = ti.n > 128;
       for (int kb = 0; kb < ti.ks; ++kb) {
         bool w = true;
         if (lane == 0) w = mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, ctrl, to, (kSiteEmpty << 24) | tag);
@@ -383,19 +383,18 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const int m = lane + 32 * j;
-          const int row = (m < kL1Feat) ? a_row0 + m : a_row_up + m;
-          cp_async_4(dA + j * 4, a_sf_base + (size_t)row * a_stride + kb * 4);
+          if (m < ti.m16) {
+            const int slot = min(ti.r0 + m, p.A - 1);
+            cp_async_4(dA + j * 4, a_sf_base + (size_t)slot * kstride + kb * 4);
+          }
         }
 #pragma unroll
-        for (int at = 0; at < 2; ++at) {
+        for (int j = 0; j < 4; ++j)
+          cp_async_4(dB + j * 4, b_sf_base + (size_t)(b_row0 + lane + 32 * j) * kstride + kb * 4);
+        if (two_sfb) {
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int n = 128 * at + 32 * j + lane;
-            if (n < ti.n) {
-              const int slot = min(ti.r0 + n, p.A - 1);
-              cp_async_4(dB + at * 512 + j * 4, b_sf_base + (size_t)slot * b_stride + kb * 4);
-            }
-          }
+          for (int j = 0; j < 4; ++j)
+            cp_async_4(dB + 512 + j * 4, b_sf_base + (size_t)(b_row1 + lane + 32 * j) * kstride + kb * 4);
         }
         cp_async_mbar_arrive_noinc(smem_u32(&full[stage]));
         ++armed;
@@ -405,10 +404,13 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
     }
     cp_async_wait<0>();
     if (lane == 0) s_misc[4] = armed;
-  } else if (warp >= 4) {
-    // ---------------- epilogue (warps 4..7 own TMEM lanes 32q .. 32q+31)
-    const int q = warp - 4;
-    uint32_t ab = 0, aphase = 0;
+  } else {
+    // ---------------- epilogue: warp w reads TMEM lanes 32q..32q+31 (token rows), q = w % 4;
+    // the warps w < 8 and w >= 8 of a quarter take the first and second half of the columns
+    const int ew = warp - 4;
+    const int q = warp & 3;
+    const int hh = ew >> 2;
+    uint32_t aphase = 0;
     int vote_buf = 0;
     TileFeed feed(s_tiles, tile_full, tile_empty);
     for (;;) {
@@ -421,105 +423,110 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
       const uint32_t tag = (uint32_t)(t < 0 ? 0 : t) & 0xFFFFFFu;
       if (t >= 0) {
         decode_tile(t, nL1, p, items, counts, offsets, ti);
-        if (lane == 0) ok = mbar_wait(smem_u32(&tfull[ab]), aphase, ctrl, to, (kSiteTmemFull << 24) | tag);
+        if (lane == 0) ok = mbar_wait(smem_u32(tfull), aphase, ctrl, to, (kSiteTmemFull << 24) | tag);
         ok = __shfl_sync(0xffffffffu, ok, 0);
       } else {
         ok = false;      // end of the feed (or abort): leave together
       }
-      // the four epilogue warps decide together, so none waits alone on a named barrier
-      if (lane == 0) s_vote[vote_buf * 4 + q] = ok ? 1 : 0;
-      named_bar_sync(3, 128);
-      const bool all_ok = s_vote[vote_buf * 4 + 0] & s_vote[vote_buf * 4 + 1] &
-                          s_vote[vote_buf * 4 + 2] & s_vote[vote_buf * 4 + 3];
+      // the epilogue warps decide together, so none waits alone on a named barrier
+      if (lane == 0) s_vote[vote_buf * kEpiWarps + ew] = ok ? 1 : 0;
+      named_bar_sync(3, 32 * kEpiWarps);
+      bool all_ok = true;
+#pragma unroll
+      for (int i = 0; i < kEpiWarps; ++i) all_ok &= s_vote[vote_buf * kEpiWarps + i] != 0;
       vote_buf ^= 1;
       if (!all_ok) break;
       tc_fence_after();
-      const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + ab * kAccStride;
-      if (ti.layer == 1) {
-        // ---- L1: pair gate (warps 0,1) with up (warps 2,3); SwiGLU; E4M3 requant
-        const int pair = q & 1;
-        const bool is_gate = q < 2;
-        float* xg = xchg + pair * 512;      // gate values of columns 8..15 [8][32]
-        float* xu = xg + 256;               // up values of columns 0..7   [8][32]
-        const int feat = ti.mt * kL1Feat + pair * 32 + lane;
-        const int sf_col = ti.mt * (kL1Feat / 32) + pair;
-        const float L = p.clamp;
-        for (int c0 = 0; c0 < ti.n; c0 += 16) {
-          float v[16];
-          tc_ld16(tbase + (uint32_t)c0, v);
-          tc_wait_ld();
-          if (is_gate) {
+      const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16);
+      const int row = q * 32 + lane;                       // token row of the block
+      const bool valid = row < ti.rows;
+      const size_t slot = (size_t)ti.r0 + row;
+      if (q * 32 < ti.rows) {                              // warp-uniform: some row of this quarter is live
+        if (ti.layer == 1) {
+          // ---- L1: 64 of the row's 128 features (blocks 2hh, 2hh+1 of 32): clamp + SwiGLU,
+          // then E4M3 + UE8M0 per 32 features, all in registers
+          const float L = p.clamp;
+          uint8_t* dst = l1a + slot * p.I + ti.nb * kL1Feat;
+          uint32_t sfw = 0;
+#pragma unroll 1
+          for (int bi = 0; bi < 2; ++bi) {
+            const int blk = 2 * hh + bi;
+            float h[32];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) xg[c * 32 + lane] = v[8 + c];
-          } else {
+            for (int half = 0; half < 2; ++half) {
+              float g[16], u[16];
+              tc_ld16(tbase + (uint32_t)(blk * 32 + half * 16), g);
+              tc_ld16(tbase + (uint32_t)(kL1Feat + blk * 32 + half * 16), u);
+              tc_wait_ld();
 #pragma unroll
-            for (int c = 0; c < 8; ++c) xu[c * 32 + lane] = v[c];
-          }
-          named_bar_sync(1 + pair, 64);
-          float g[8], u[8];
-          if (is_gate) {
-#pragma unroll
-            for (int c = 0; c < 8; ++c) { g[c] = v[c]; u[c] = xu[c * 32 + lane]; }
-          } else {
-#pragma unroll
-            for (int c = 0; c < 8; ++c) { g[c] = xg[c * 32 + lane]; u[c] = v[8 + c]; }
-          }
-          named_bar_sync(1 + pair, 64);
-          const int cb = c0 + (is_gate ? 0 : 8);
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const int col = cb + c;
-            if (col >= ti.rows) break;
-            float gg = g[c], uu = u[c];
-            if (p.use_clamp) {
-              gg = fminf(gg, L);
-              uu = fminf(fmaxf(uu, -L), L);
+              for (int i = 0; i < 16; ++i) {
+                float gg = g[i], uu = u[i];
+                if (p.use_clamp) {
+                  gg = fminf(gg, L);
+                  uu = fminf(fmaxf(uu, -L), L);
+                }
+                h[half * 16 + i] = gg * __fdividef(1.0f, 1.0f + __expf(-gg)) * uu;   // fast-math SiLU
+              }
             }
-            const float h = gg * __fdividef(1.0f, 1.0f + __expf(-gg)) * uu;   // fast-math SiLU
-            float a = fabsf(h);
+            float a = 0.f;
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+            for (int i = 0; i < 32; ++i) a = fmaxf(a, fabsf(h[i]));
             const int s = block_scale_exp<true>(a);
-            const uint32_t code = e4m3_code(h * exp2_neg(s));
-            const size_t slot = (size_t)(ti.r0 + col);
-            l1a[slot * p.I + feat] = (uint8_t)code;
-            if (lane == 0) l1a_sf[slot * (p.I / 32) + sf_col] = (uint8_t)(s + 127);
-          }
-        }
-      } else {
-        // ---- L2: weight by topk_w, bf16 rows indexed by the flat assignment
-        const int hrow = ti.mt * kL2Rows + q * 32 + lane;
-        for (int c0 = 0; c0 < ti.n; c0 += 16) {
-          float v[16];
-          tc_ld16(tbase + (uint32_t)c0, v);
-          tc_wait_ld();
-          const int mc = c0 + (lane & 15);
-          int f = 0;
-          float w = 0.f;
-          if (mc < ti.rows) {
-            f = __ldg(perm + ti.r0 + mc);
-            w = __ldg(p.topk_w + f);
-          }
+            const float inv = exp2_neg(s);
+            uint32_t w[8];
 #pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            if (c0 + c >= ti.rows) break;
-            const int fc = __shfl_sync(0xffffffffu, f, c);
-            const float wc = __shfl_sync(0xffffffffu, w, c);
-            stage_out[(size_t)fc * p.H + hrow] = v[c] * wc;
+            for (int i = 0; i < 8; ++i)
+              w[i] = e4m3_code(h[4 * i] * inv) | (e4m3_code(h[4 * i + 1] * inv) << 8) |
+                     (e4m3_code(h[4 * i + 2] * inv) << 16) | (e4m3_code(h[4 * i + 3] * inv) << 24);
+            if (valid) {
+              uint4* d4 = reinterpret_cast<uint4*>(dst + blk * 32);
+              d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+              d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+            }
+            sfw |= (uint32_t)(s + 127) << (8 * bi);
+          }
+          if (valid)
+            *reinterpret_cast<uint16_t*>(l1a_sf + slot * (p.I / 32) + ti.nb * (kL1Feat / 32) + 2 * hh) =
+                (uint16_t)sfw;
+        } else {
+          // ---- L2: half of the row's N hidden outputs x top-k weight -> fp32 row of the flat assignment
+          int f = 0;
+          float wt = 0.f;
+          if (valid) {
+            f = __ldg(perm + slot);
+            wt = __ldg(p.topk_w + f);
+          }
+          const int nh = ti.n >> 1;
+          const int c_beg = hh * nh;
+          float* dst = stage_out + (size_t)f * p.H + ti.nb * kTileN;
+#pragma unroll 1
+          for (int c0 = c_beg; c0 < c_beg + nh; c0 += 32) {
+            float v[16], v2[16];
+            tc_ld16(tbase + (uint32_t)c0, v);
+            tc_ld16(tbase + (uint32_t)(c0 + 16), v2);
+            tc_wait_ld();
+            if (valid) {
+              float4* d4 = reinterpret_cast<float4*>(dst + c0);
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                d4[i] = make_float4(v[4 * i] * wt, v[4 * i + 1] * wt, v[4 * i + 2] * wt, v[4 * i + 3] * wt);
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                d4[4 + i] = make_float4(v2[4 * i] * wt, v2[4 * i + 1] * wt, v2[4 * i + 2] * wt, v2[4 * i + 3] * wt);
+            }
           }
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&tempty[ab]));
+      if (lane == 0) mbar_arrive(smem_u32(tempty));
       if (ti.layer == 1) {
         fence_proxy_async_global();
         __threadfence();
-        named_bar_sync(3, 128);
-        if (q == 0 && lane == 0) red_release_add(&l1_done[ti.e], 1u);
+        named_bar_sync(3, 32 * kEpiWarps);
+        if (ew == 0 && lane == 0) red_release_add(&l1_done[ti.e], 1u);
       }
-      ab ^= 1u;
-      if (ab == 0) aphase ^= 1u;
+      aphase ^= 1u;
     }
     __threadfence();
   }
@@ -529,14 +536,15 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
   if (threadIdx.x == 0) {
     // After an abort, TMA loads may still be landing.  Each issued but
     // unconsumed stage's barrier completes once its bytes land, provided the
-    // 32 scale-loader arrivals were made; make the missing ones here.
+    // 32 scale-loader arrivals and both producers' arrivals were made; make
+    // the missing ones here (a producer that stopped early: its arrival, no bytes).
     const uint32_t issued0 = s_misc[2], issued1 = s_misc[5], consumed = s_misc[1], armed = s_misc[4];
     const uint32_t issued = issued0 > issued1 ? issued0 : issued1;
     for (uint32_t s = consumed; s < issued; ++s) {
       const uint32_t bar = smem_u32(&full[s % kStages]);
       if (s >= armed)
         for (int i = 0; i < 32; ++i) mbar_arrive(bar);
-      if (s >= issued0) mbar_arrive(bar);      // a producer that stopped early: its arrival, no bytes
+      if (s >= issued0) mbar_arrive(bar);
       if (s >= issued1) mbar_arrive(bar);
       if (!mbar_wait_drain(bar, (s / kStages) & 1u, to)) set_error(ctrl, MM_ERR_TIMEOUT, kSiteDrain << 24);
     }
@@ -594,39 +602,15 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
 }
 
 // ---------------------------------------------------------------- host side
-// Template kernels are configured and launched in the translation unit that
-// defines them.
-int layer_smem_bytes(int variant) {
-  return variant == kVariantThin ? ThinVariant::kSmemBytes
-       : variant == kVariantNarrow ? NarrowVariant::kSmemBytes : WideVariant::kSmemBytes;
-}
-
-int layer_max_n(int variant) {
-  return variant == kVariantThin ? ThinVariant::kMaxN
-       : variant == kVariantNarrow ? NarrowVariant::kMaxN : WideVariant::kMaxN;
-}
-
-cudaError_t layer_prepare(int variant, int* ctas_per_sm) {
-  const void* fn = variant == kVariantThin ? (const void*)megamoe_kernel<ThinVariant>
-                 : variant == kVariantNarrow ? (const void*)megamoe_kernel<NarrowVariant>
-                                             : (const void*)megamoe_kernel<WideVariant>;
-  const int smem = layer_smem_bytes(variant);
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+cudaError_t layer_prepare(int* ctas_per_sm) {
+  cudaError_t e = cudaFuncSetAttribute(megamoe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, fn, kThreads, smem);
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, megamoe_kernel, kThreads, kSmemBytes);
 }
 
-cudaError_t layer_launch(int variant, int grid, cudaStream_t stream, const CUtensorMap& tm_w1,
-                         const CUtensorMap& tm_w2, const CUtensorMap& tm_xs, const CUtensorMap& tm_l1a,
-                         const ForwardParams& p) {
-  if (variant == kVariantThin)
-    megamoe_kernel<ThinVariant><<<grid, kThreads, ThinVariant::kSmemBytes, stream>>>(tm_w1, tm_w2, tm_xs, tm_l1a, p);
-  else if (variant == kVariantNarrow)
-    megamoe_kernel<NarrowVariant><<<grid, kThreads, NarrowVariant::kSmemBytes, stream>>>(tm_w1, tm_w2, tm_xs,
-                                                                                         tm_l1a, p);
-  else
-    megamoe_kernel<WideVariant><<<grid, kThreads, WideVariant::kSmemBytes, stream>>>(tm_w1, tm_w2, tm_xs,
-                                                                                     tm_l1a, p);
+// maps: W1, W2, dispatched tokens (16- and 128-row boxes), L1 activations (16- and 128-row boxes)
+cudaError_t layer_launch(int grid, cudaStream_t stream, const CUtensorMap* maps, const ForwardParams& p) {
+  megamoe_kernel<<<grid, kThreads, kSmemBytes, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p);
   return cudaGetLastError();
 }
 
