@@ -11,8 +11,9 @@
 
 namespace mm {
 __global__ void route_kernel(const RouteParams p);
-cudaError_t layer_prepare(int* ctas_per_sm);
-cudaError_t layer_launch(int grid, cudaStream_t stream, const CUtensorMap* maps, const ForwardParams& p);
+int layer_max_rows(int variant);
+cudaError_t layer_prepare(int variant, int* ctas_per_sm);
+cudaError_t layer_launch(int variant, int grid, cudaStream_t stream, const CUtensorMap* maps, const ForwardParams& p);
 cudaError_t launch_quantize(const float* src, long long nblocks, bool e4m3, uint8_t* dst, uint8_t* sf,
                             int grid, cudaStream_t stream);
 }  // namespace mm
@@ -58,8 +59,15 @@ int check_shape(long long T, int E, int k, int H, int I) {
 struct DevState {
   bool ready = false;
   int sms = 0;
-  int max_resident = 0;   // layer kernel CTAs resident at once
+  int max_resident[kNumVariants] = {0, 0};   // layer kernel CTAs resident at once, per variant
 };
+
+// Kernel variant for a batch: with at most 16 assignments per expert on
+// average (decode), the thin variant's deeper weight ring; otherwise the wide
+// variant's 128-token tiles.
+int pick_variant(long long assignments, int experts) {
+  return assignments <= 16ll * experts ? kVariantThin : kVariantWide;
+}
 std::mutex g_mu;
 DevState g_dev[128];
 
@@ -92,12 +100,14 @@ int device_state(int* dev_out, DevState** st_out) {
       cudaGetLastError();
       return MM_ERR_CUDA;
     }
-    int per_sm = 0;
-    if (layer_prepare(&per_sm) != cudaSuccess) {
-      cudaGetLastError();
-      return MM_ERR_CUDA;
+    for (int v = 0; v < kNumVariants; ++v) {
+      int per_sm = 0;
+      if (layer_prepare(v, &per_sm) != cudaSuccess) {
+        cudaGetLastError();
+        return MM_ERR_CUDA;
+      }
+      st.max_resident[v] = per_sm * prop.multiProcessorCount;
     }
-    st.max_resident = per_sm * prop.multiProcessorCount;
     st.sms = prop.multiProcessorCount;
     st.ready = true;
   }
@@ -121,7 +131,7 @@ int encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t
 int launch_route(int T, int E, int k, const int32_t* topk_idx, uint8_t* ws, const Layout& L, cudaStream_t st) {
   RouteParams rp;
   rp.T = T; rp.E = E; rp.k = k; rp.A = T * k;
-  rp.max_n = kTileM;
+  rp.max_n = layer_max_rows(pick_variant((long long)T * k, E));
   rp.topk_idx = topk_idx;
   rp.ws = ws;
   rp.L = L;
@@ -196,7 +206,8 @@ int mm_forward(int num_tokens, int experts, int topk, int hidden, int inter,
   DevState* st;
   rc = device_state(&dev, &st);
   if (rc != MM_OK) return rc;
-  const int grid = mm_grid_size(st->sms, reserved_now(), num_sms, st->max_resident);
+  const int variant = pick_variant((long long)T * k, E);
+  const int grid = mm_grid_size(st->sms, reserved_now(), num_sms, st->max_resident[variant]);
   const int A = T * k;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
 
@@ -237,7 +248,7 @@ int mm_forward(int num_tokens, int experts, int topk, int hidden, int inter,
   fp.y = static_cast<uint16_t*>(y);
   fp.ws = ws;
   fp.L = L;
-  if (layer_launch(grid, s, maps, fp) != cudaSuccess) return MM_ERR_CUDA;
+  if (layer_launch(variant, grid, s, maps, fp) != cudaSuccess) return MM_ERR_CUDA;
   return MM_OK;
 }
 

@@ -20,22 +20,53 @@ constexpr int kBlockK = 128;        // K per pipeline stage: 4 UE8M0 scale block
 constexpr int kTileM = 128;         // MMA M: tokens per tile
 constexpr int kTileN = 256;         // MMA N: weight rows per tile
 constexpr int kL1Feat = 128;        // intermediate features per L1 tile (128 gate + 128 up rows)
-constexpr int kStages = 4;          // shared-memory ring depth
 constexpr int kEpiWarps = 8;        // epilogue warps: two per 32-lane TMEM quarter
 constexpr int kThreads = 32 * (4 + kEpiWarps);   // producer, MMA, scale loader, producer, epilogue
 
-constexpr int kABytes = kTileM * kBlockK;           // 16 KB: 128 token rows x 128 E4M3 bytes
 constexpr int kBBytes = kTileN * kBlockK;           // 32 KB: 256 weight rows x 128 padded FP4 bytes
 // A packed-FP4 TMA box counts its global (packed) bytes toward the barrier's
 // transaction count, not its padded shared-memory footprint.
 constexpr int kBHalfTxBytes = 128 * kBlockK / 2;    // 8 KB: one 128-row weight box
 constexpr int kSFABytes = 512;                      // one 128-row scale atom (tokens)
 constexpr int kSFBBytes = 1024;                     // two 128-row scale atoms (weights)
-constexpr int kStageBytes = kABytes + kBBytes + kSFABytes + kSFBBytes;
 constexpr int kBarBytes = 512;                      // mbarriers + small shared state
-constexpr int kSmemBytes = kStages * kStageBytes + kBarBytes + 1024 /*align*/;
-static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
-static_assert(kABytes % 1024 == 0 && kBBytes % 1024 == 0, "SW128 tiles need 1 KB alignment");
+
+// Tile ring of the dynamic schedule: depth, and the number of roles that read
+// each entry (producer 1, scale loader, MMA issuer, the epilogue warps).
+constexpr int kTileRing = 4;
+constexpr int kTileReaders = 1 + 1 + 1 + kEpiWarps;
+
+// A kernel variant: the token rows a shared-memory stage holds and the ring
+// depth.  The MMA always reads 128 token rows from a stage's A address; the
+// thin variant keeps only 32 rows per stage, so rows 32..127 of its MMA read
+// whatever follows in shared memory and land in accumulator lanes that no
+// epilogue thread reads.  Its ring is half again as deep, which is what a
+// decode batch (a few tokens per expert, weight streaming) needs.  The wide
+// variant adds the epilogue's transpose buffers (see kXposeBytes).
+template <int kARows_, int kStages_, bool kXpose_>
+struct Variant {
+  static constexpr int kARows = kARows_;
+  static constexpr int kStages = kStages_;
+  static constexpr bool kXpose = kXpose_;
+  static constexpr int kABytes = kARows * kBlockK;
+  static constexpr int kStageBytes = kABytes + kBBytes + kSFABytes + kSFBBytes;
+  // Epilogue transpose buffer per warp: 32 token rows x 16 fp32 columns, so the
+  // L2 epilogue stores whole 64-byte row segments instead of 16-byte pieces of
+  // 32 different rows.
+  static constexpr int kXposeBytes = kXpose ? kEpiWarps * 32 * 16 * 4 : 0;
+  static constexpr int kSmemBytes = kStages * kStageBytes + kXposeBytes + kBarBytes + 1024 /*align*/;
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+  static_assert(kABytes % 1024 == 0 && kBBytes % 1024 == 0, "SW128 tiles need 1 KB alignment");
+  static_assert(kARows % 16 == 0 && kARows <= kTileM, "token rows per stage");
+  // barriers (2 per stage, 3 accumulator/drain, 2 per tile-ring slot), misc words, votes, tile ring
+  static_assert((2 * kStages + 3 + 2 * kTileRing) * 8 + 8 * 4 + 2 * kEpiWarps * 4 + kTileRing * 9 * 4 <= kBarBytes,
+                "barrier region");
+  // the MMA's 128-row A window of the last stage stays inside the allocation
+  static_assert((kStages - 1) * kABytes + kTileM * kBlockK <= kStages * kStageBytes, "A window");
+};
+using WideVariant = Variant<128, 4, true>;
+using ThinVariant = Variant<32, 6, false>;
+enum VariantId : int { kVariantWide = 0, kVariantThin = 1, kNumVariants = 2 };
 
 // TMEM columns: one 256-column fp32 accumulator, then the scale factors of the
 // stage in flight (two accumulators and the scales would need 524 columns).
@@ -49,12 +80,6 @@ enum CtrlWord : int {
   kStatus = 0, kErrSm = 1, kErrInfo = 2, kAbort = 3, kGridBar = 4, kSiteMask = 5, kNextTile = 6, kCtrlWords = 64
 };
 
-// Tile-index ring of the dynamic schedule: depth, and the number of roles that
-// read each entry (producer 1, scale loader, MMA issuer, the epilogue warps).
-constexpr int kTileRing = 4;
-constexpr int kTileReaders = 1 + 1 + 1 + kEpiWarps;
-static_assert((3 * kStages + 3 + 2 * kTileRing) * 8 + 8 * 4 + 2 * kEpiWarps * 4 + kTileRing * 4 <= kBarBytes,
-              "barrier region");
 
 // Wait sites recorded in the error info word (site << 24 | tile & 0xFFFFFF).
 enum WaitSite : uint32_t {

@@ -56,6 +56,7 @@ struct Tile {
   int m16;     // rows rounded up to 16: token rows loaded
   int n;       // MMA N: 256, or 128 for a hidden tail
   int ks;      // K stages
+  int tag;     // tile index (reported with a wait that gives up)
 };
 
 // Tiles are numbered L1 first, then L2; within a layer expert-major, then the
@@ -88,38 +89,67 @@ __device__ __forceinline__ void decode_tile(int t, int nL1, const ForwardParams&
   ti.m16 = (ti.rows + 15) & ~15;
   ti.n = l1 ? kTileN : min(kTileN, p.H - nb * kTileN);
   ti.ks = l1 ? p.ks1 : p.ks2;
+  ti.tag = t & 0xFFFFFF;
 }
 
 // Dynamic tile schedule.  Producer 0 claims the next tile index from a global
-// counter (reset by the routing kernel of the same launch) and publishes it in
-// a small shared-memory ring; every other role takes the indices from the ring
-// in the same order.  A negative index ends the stream.  Tiles are claimed in
-// increasing index order (all L1 tiles before any L2 tile, expert-major), so an
-// L2 tile only waits for L1 tiles that running CTAs have already claimed.
+// counter (reset by the routing kernel of the same launch), decodes it and
+// publishes the decoded tile in a small shared-memory ring; every other role
+// takes the tiles from the ring in the same order.  layer == 0 ends the
+// stream.  The atomic for the next tile is issued as soon as the current one
+// is published, so its round trip overlaps the current tile's loads.
+// Tiles are claimed in increasing index order (all L1 tiles before any L2
+// tile, expert-major) and L1 tiles wait only for the dispatch, so the oldest
+// unfinished L1 tile is always either running or held (claimed ahead) by a CTA
+// whose running tile is an L1 tile or an L2 tile of a larger index: no cycle of
+// waits can form.
 struct TileFeed {
-  int32_t* ring;
+  Tile* ring;
   uint64_t* full;
   uint64_t* empty;
   uint32_t i = 0;
-  __device__ TileFeed(int32_t* r, uint64_t* f, uint64_t* e) : ring(r), full(f), empty(e) {}
+  int ahead = -1;              // producer 0: index claimed for the next publication
+  __device__ TileFeed(Tile* r, uint64_t* f, uint64_t* e) : ring(r), full(f), empty(e) {}
 
-  __device__ int claim(uint32_t* counter, int total, uint32_t* ctrl, unsigned long long to, bool& ok) {
+  // Producer 0: claim, decode, publish.  Returns false at the end of the stream or on abort (ok = false).
+  __device__ bool claim(uint32_t* counter, int total, int nL1, const ForwardParams& p, const int32_t* items,
+                        const int32_t* counts, const int32_t* offsets, uint32_t* ctrl, unsigned long long to,
+                        bool& ok, Tile& ti) {
     const uint32_t slot = i % kTileRing, ph = (i / kTileRing) & 1u;
     ++i;
-    if (!mbar_wait(smem_u32(&empty[slot]), ph ^ 1u, ctrl, to, kSiteTileRing << 24)) { ok = false; return -1; }
-    const int t = (int)atomicAdd(counter, 1u);
-    const int v = t < total ? t : -1;
-    ring[slot] = v;
-    mbar_arrive(smem_u32(&full[slot]));          // release: the index is visible to the readers
-    return v;
+    if (!mbar_wait(smem_u32(&empty[slot]), ph ^ 1u, ctrl, to, kSiteTileRing << 24)) { ok = false; return false; }
+    const int t = ahead >= 0 ? ahead : (int)atomicAdd(counter, 1u);
+    if (t < total) decode_tile(t, nL1, p, items, counts, offsets, ti);
+    else ti.layer = 0;
+    ring[slot] = ti;
+    mbar_arrive(smem_u32(&full[slot]));          // release: the tile is visible to the readers
+    ahead = t < total ? (int)atomicAdd(counter, 1u) : -1;   // consumed at the next claim
+    return ti.layer != 0;
   }
-  __device__ int take(uint32_t* ctrl, unsigned long long to, bool& ok) {
+  // One reading thread.
+  __device__ bool take(uint32_t* ctrl, unsigned long long to, bool& ok, Tile& ti) {
     const uint32_t slot = i % kTileRing, ph = (i / kTileRing) & 1u;
     ++i;
-    if (!mbar_wait(smem_u32(&full[slot]), ph, ctrl, to, kSiteTileRing << 24)) { ok = false; return -1; }
-    const int v = ring[slot];
+    if (!mbar_wait(smem_u32(&full[slot]), ph, ctrl, to, kSiteTileRing << 24)) { ok = false; return false; }
+    ti = ring[slot];
     mbar_arrive(smem_u32(&empty[slot]));
-    return v;
+    return ti.layer != 0;
+  }
+  // A whole warp: lane 0 waits, every lane then observes the completed phase
+  // itself (it stays complete until this warp's arrival frees the slot) and
+  // reads the tile; lane 0 frees the slot after the warp has read it.
+  __device__ bool take_warp(int lane, uint32_t* ctrl, unsigned long long to, bool& ok, Tile& ti) {
+    const uint32_t slot = i % kTileRing, ph = (i / kTileRing) & 1u;
+    ++i;
+    bool w = true;
+    if (lane == 0) w = mbar_wait(smem_u32(&full[slot]), ph, ctrl, to, kSiteTileRing << 24);
+    w = __shfl_sync(0xffffffffu, w, 0);
+    if (!w) { ok = false; return false; }
+    (void)mbar_try_wait(smem_u32(&full[slot]), ph);
+    ti = ring[slot];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&empty[slot]));
+    return ti.layer != 0;
   }
 };
 
@@ -135,18 +165,22 @@ __device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" :: "r"(bar) : "memory");
 }
 
+template <class V>
 __global__ void __launch_bounds__(kThreads, 1)
 megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant__ CUtensorMap tm_w2,
                const __grid_constant__ CUtensorMap tm_xs16, const __grid_constant__ CUtensorMap tm_xs128,
                const __grid_constant__ CUtensorMap tm_l1a16, const __grid_constant__ CUtensorMap tm_l1a128,
                const __grid_constant__ ForwardParams p) {
+  constexpr int kStages = V::kStages;
+  constexpr int kABytes = V::kABytes;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = sm;                                   // [kStages] token rows
   uint8_t* sB = sA + kStages * kABytes;               // [kStages] weight rows
   uint8_t* sSFA = sB + kStages * kBBytes;             // [kStages] token scale atom
   uint8_t* sSFB = sSFA + kStages * kSFABytes;         // [kStages] two weight scale atoms
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sSFB + kStages * kSFBBytes);
+  float* sX = reinterpret_cast<float*>(sSFB + kStages * kSFBBytes);   // [kEpiWarps] transpose buffers
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sSFB + kStages * kSFBBytes + V::kXposeBytes);
   uint64_t* full = bars;                     // [kStages] TMA bytes + 32 scale-loader lanes' cp.async landed
   uint64_t* empty = bars + kStages;          // [kStages] MMAs reading the stage are done
   uint64_t* tfull = bars + 2 * kStages;      // accumulator ready
@@ -158,7 +192,7 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
   // loader), stages issued (producer 1)
   uint32_t* s_misc = reinterpret_cast<uint32_t*>(tile_empty + kTileRing);
   int32_t* s_vote = reinterpret_cast<int32_t*>(s_misc + 8);    // epilogue votes [2][kEpiWarps]
-  int32_t* s_tiles = s_vote + 2 * kEpiWarps;                   // [kTileRing] claimed tile indices
+  Tile* s_tiles = reinterpret_cast<Tile*>(s_vote + 2 * kEpiWarps);   // [kTileRing] claimed tiles
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint32_t* ctrl = reinterpret_cast<uint32_t*>(p.ws + p.L.ctrl);
@@ -244,21 +278,26 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
       // arms the stage's barrier with its own bytes.
       const int pid = warp == 0 ? 0 : 1;
       uint32_t stage = 0, phase = 0, issued = 0;
+      int ready_key = -1;            // (layer, expert) whose dependency was last seen satisfied
       bool ok = true;
       TileFeed feed(s_tiles, tile_full, tile_empty);
       while (ok) {
-        const int t = pid == 0 ? feed.claim(&ctrl[kNextTile], total, ctrl, to, ok) : feed.take(ctrl, to, ok);
-        if (t < 0) break;
         Tile ti;
-        decode_tile(t, nL1, p, items, counts, offsets, ti);
-        const uint32_t tag = (uint32_t)t & 0xFFFFFFu;
-        if (ti.layer == 1)
-          ok = counter_wait(&arrival[ti.e], (uint32_t)__ldg(counts + ti.e), ctrl, to, (kSiteArrival << 24) | tag);
-        else
-          ok = counter_wait(&l1_done[ti.e], l1_tiles_of(items, ti.e, p.mt1), ctrl, to, (kSiteL1Done << 24) | tag);
-        if (!ok) break;
-        fence_proxy_async_global();
-        const bool full_box = p.a_box128 && ti.m16 == kTileM;
+        const bool more = pid == 0 ? feed.claim(&ctrl[kNextTile], total, nL1, p, items, counts, offsets, ctrl, to, ok, ti)
+                                   : feed.take(ctrl, to, ok, ti);
+        if (!more) break;
+        const uint32_t tag = (uint32_t)ti.tag;
+        const int key = ti.e * 2 + ti.layer - 1;
+        if (key != ready_key) {
+          if (ti.layer == 1)
+            ok = counter_wait(&arrival[ti.e], (uint32_t)__ldg(counts + ti.e), ctrl, to, (kSiteArrival << 24) | tag);
+          else
+            ok = counter_wait(&l1_done[ti.e], l1_tiles_of(items, ti.e, p.mt1), ctrl, to, (kSiteL1Done << 24) | tag);
+          if (!ok) break;
+          fence_proxy_async_global();
+          ready_key = key;
+        }
+        const bool full_box = V::kARows == kTileM && p.a_box128 && ti.m16 == kTileM;
         const int nbox = ti.m16 / 16;
         const int my_a_bytes = full_box ? (pid == 0 ? kABytes : 0) : ((nbox + 1 - pid) / 2) * 16 * kBlockK;
         const bool my_b = pid == 0 || ti.n > 128;
@@ -302,11 +341,9 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
       bool ok = true;
       TileFeed feed(s_tiles, tile_full, tile_empty);
       while (ok) {
-        const int t = feed.take(ctrl, to, ok);
-        if (t < 0) break;
         Tile ti;
-        decode_tile(t, nL1, p, items, counts, offsets, ti);
-        const uint32_t tag = (uint32_t)t & 0xFFFFFFu;
+        if (!feed.take(ctrl, to, ok, ti)) break;
+        const uint32_t tag = (uint32_t)ti.tag;
         if (!mbar_wait(smem_u32(tempty), aphase ^ 1u, ctrl, to, (kSiteTmemEmpty << 24) | tag)) break;
         tc_fence_after();
         const uint32_t id0 = idesc_mx((uint32_t)ti.n, 0u);
@@ -344,28 +381,29 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
   } else if (warp == 2) {
     // ---------------- scale loader (32 lanes)
     uint32_t stage = 0, phase = 0, armed = 0;
+    int ready_key = -1;
     const int H32 = p.H / 32, I32 = p.I / 32;
     TileFeed feed(s_tiles, tile_full, tile_empty);
     for (;;) {
       bool fed = true;
-      int t = -1;
-      if (lane == 0) t = feed.take(ctrl, to, fed);
-      t = __shfl_sync(0xffffffffu, t, 0);
-      if (t < 0) break;
       Tile ti;
-      decode_tile(t, nL1, p, items, counts, offsets, ti);
-      const uint32_t tag = (uint32_t)t & 0xFFFFFFu;
+      if (!feed.take_warp(lane, ctrl, to, fed, ti)) break;
+      const uint32_t tag = (uint32_t)ti.tag;
       bool ok = true;
-      if (lane == 0) {
-        ok = (ti.layer == 1)
-                 ? counter_wait(&arrival[ti.e], (uint32_t)__ldg(counts + ti.e), ctrl, to, (kSiteArrival << 24) | tag)
-                 : counter_wait(&l1_done[ti.e], l1_tiles_of(items, ti.e, p.mt1), ctrl, to, (kSiteL1Done << 24) | tag);
+      const int key = ti.e * 2 + ti.layer - 1;
+      if (key != ready_key) {
+        if (lane == 0) {
+          ok = (ti.layer == 1)
+                   ? counter_wait(&arrival[ti.e], (uint32_t)__ldg(counts + ti.e), ctrl, to, (kSiteArrival << 24) | tag)
+                   : counter_wait(&l1_done[ti.e], l1_tiles_of(items, ti.e, p.mt1), ctrl, to, (kSiteL1Done << 24) | tag);
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        __syncwarp();
+        // every lane acquires the producers' writes before reading them
+        if (ti.layer == 1) (void)ld_acquire(&arrival[ti.e]); else (void)ld_acquire(&l1_done[ti.e]);
+        ready_key = key;
       }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-      __syncwarp();
-      // every lane acquires the producers' writes before reading them
-      if (ti.layer == 1) (void)ld_acquire(&arrival[ti.e]); else (void)ld_acquire(&l1_done[ti.e]);
       // A: the block's token rows; B: the tile's weight rows in two 128-row atoms
       const uint8_t* a_sf_base = ti.layer == 1 ? xs_sf : l1a_sf;
       const uint8_t* b_sf_base = ti.layer == 1 ? p.w1_sf : p.w2_sf;
@@ -415,15 +453,9 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
     TileFeed feed(s_tiles, tile_full, tile_empty);
     for (;;) {
       bool ok = true;
-      int t = -1;
-      if (lane == 0) t = feed.take(ctrl, to, ok);
-      t = __shfl_sync(0xffffffffu, t, 0);
-      ok = __shfl_sync(0xffffffffu, ok, 0);
       Tile ti;
-      const uint32_t tag = (uint32_t)(t < 0 ? 0 : t) & 0xFFFFFFu;
-      if (t >= 0) {
-        decode_tile(t, nL1, p, items, counts, offsets, ti);
-        if (lane == 0) ok = mbar_wait(smem_u32(tfull), aphase, ctrl, to, (kSiteTmemFull << 24) | tag);
+      if (feed.take_warp(lane, ctrl, to, ok, ti)) {
+        if (lane == 0) ok = mbar_wait(smem_u32(tfull), aphase, ctrl, to, (kSiteTmemFull << 24) | (uint32_t)ti.tag);
         ok = __shfl_sync(0xffffffffu, ok, 0);
       } else {
         ok = false;      // end of the feed (or abort): leave together
@@ -498,21 +530,59 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
           }
           const int nh = ti.n >> 1;
           const int c_beg = hh * nh;
-          float* dst = stage_out + (size_t)f * p.H + ti.nb * kTileN;
+          if constexpr (V::kXpose) {
+            // 16 columns at a time pass through this warp's transpose buffer (32 rows x four
+            // 16-byte chunks; chunk c of row r sits at position c ^ ((r >> 1) & 3), which keeps
+            // both the row-wise writes and the column-wise reads free of bank conflicts); lane l
+            // then stores chunk l % 4 of rows l / 4 + 8i, whole 64-byte row segments.
+            float4* xb = reinterpret_cast<float4*>(sX + ew * (32 * 16));
+            const int rr = lane >> 2, cc = lane & 3;
+            float* dst[4];
+            bool live[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int r = rr + 8 * i;
+              const int fr = __shfl_sync(0xffffffffu, f, r);
+              live[i] = q * 32 + r < ti.rows;
+              dst[i] = stage_out + (size_t)fr * p.H + ti.nb * kTileN + 4 * cc;
+            }
+            const int wsw = (lane >> 1) & 3;
 #pragma unroll 1
-          for (int c0 = c_beg; c0 < c_beg + nh; c0 += 32) {
-            float v[16], v2[16];
-            tc_ld16(tbase + (uint32_t)c0, v);
-            tc_ld16(tbase + (uint32_t)(c0 + 16), v2);
-            tc_wait_ld();
-            if (valid) {
-              float4* d4 = reinterpret_cast<float4*>(dst + c0);
+            for (int c0 = c_beg; c0 < c_beg + nh; c0 += 16) {
+              float v[16];
+              tc_ld16(tbase + (uint32_t)c0, v);
+              tc_wait_ld();
 #pragma unroll
-              for (int i = 0; i < 4; ++i)
-                d4[i] = make_float4(v[4 * i] * wt, v[4 * i + 1] * wt, v[4 * i + 2] * wt, v[4 * i + 3] * wt);
+              for (int j = 0; j < 4; ++j)
+                xb[lane * 4 + (j ^ wsw)] =
+                    make_float4(v[4 * j] * wt, v[4 * j + 1] * wt, v[4 * j + 2] * wt, v[4 * j + 3] * wt);
+              __syncwarp();
 #pragma unroll
-              for (int i = 0; i < 4; ++i)
-                d4[4 + i] = make_float4(v2[4 * i] * wt, v2[4 * i + 1] * wt, v2[4 * i + 2] * wt, v2[4 * i + 3] * wt);
+              for (int i = 0; i < 4; ++i) {
+                const int r = rr + 8 * i;
+                const float4 val = xb[r * 4 + (cc ^ ((r >> 1) & 3))];
+                if (live[i]) *reinterpret_cast<float4*>(dst[i] + c0) = val;
+              }
+              __syncwarp();
+            }
+          } else {
+            // few rows per tile: each thread stores its own row directly
+            float* dst = stage_out + (size_t)f * p.H + ti.nb * kTileN;
+#pragma unroll 1
+            for (int c0 = c_beg; c0 < c_beg + nh; c0 += 32) {
+              float v[16], v2[16];
+              tc_ld16(tbase + (uint32_t)c0, v);
+              tc_ld16(tbase + (uint32_t)(c0 + 16), v2);
+              tc_wait_ld();
+              if (valid) {
+                float4* d4 = reinterpret_cast<float4*>(dst + c0);
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                  d4[i] = make_float4(v[4 * i] * wt, v[4 * i + 1] * wt, v[4 * i + 2] * wt, v[4 * i + 3] * wt);
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                  d4[4 + i] = make_float4(v2[4 * i] * wt, v2[4 * i + 1] * wt, v2[4 * i + 2] * wt, v2[4 * i + 3] * wt);
+              }
             }
           }
         }
@@ -536,8 +606,9 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
   if (threadIdx.x == 0) {
     // After an abort, TMA loads may still be landing.  Each issued but
     // unconsumed stage's barrier completes once its bytes land, provided the
-    // 32 scale-loader arrivals and both producers' arrivals were made; make
-    // the missing ones here (a producer that stopped early: its arrival, no bytes).
+    // scale loader's 32 arrivals and both producers' arrivals were made; make
+    // the missing ones here (a role that stopped early: its arrival, no
+    // bytes; the scale loader has already waited for its own copies).
     const uint32_t issued0 = s_misc[2], issued1 = s_misc[5], consumed = s_misc[1], armed = s_misc[4];
     const uint32_t issued = issued0 > issued1 ? issued0 : issued1;
     for (uint32_t s = consumed; s < issued; ++s) {
@@ -602,15 +673,27 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
 }
 
 // ---------------------------------------------------------------- host side
-cudaError_t layer_prepare(int* ctas_per_sm) {
-  cudaError_t e = cudaFuncSetAttribute(megamoe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+// Template kernels are configured and launched in the translation unit that
+// defines them.
+int layer_max_rows(int variant) { return variant == kVariantThin ? ThinVariant::kARows : WideVariant::kARows; }
+
+cudaError_t layer_prepare(int variant, int* ctas_per_sm) {
+  const void* fn = variant == kVariantThin ? (const void*)megamoe_kernel<ThinVariant>
+                                           : (const void*)megamoe_kernel<WideVariant>;
+  const int smem = variant == kVariantThin ? ThinVariant::kSmemBytes : WideVariant::kSmemBytes;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, megamoe_kernel, kThreads, kSmemBytes);
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, fn, kThreads, smem);
 }
 
 // maps: W1, W2, dispatched tokens (16- and 128-row boxes), L1 activations (16- and 128-row boxes)
-cudaError_t layer_launch(int grid, cudaStream_t stream, const CUtensorMap* maps, const ForwardParams& p) {
-  megamoe_kernel<<<grid, kThreads, kSmemBytes, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p);
+cudaError_t layer_launch(int variant, int grid, cudaStream_t stream, const CUtensorMap* maps, const ForwardParams& p) {
+  if (variant == kVariantThin)
+    megamoe_kernel<ThinVariant><<<grid, kThreads, ThinVariant::kSmemBytes, stream>>>(maps[0], maps[1], maps[2],
+                                                                                     maps[3], maps[4], maps[5], p);
+  else
+    megamoe_kernel<WideVariant><<<grid, kThreads, WideVariant::kSmemBytes, stream>>>(maps[0], maps[1], maps[2],
+                                                                                     maps[3], maps[4], maps[5], p);
   return cudaGetLastError();
 }
 
