@@ -36,6 +36,14 @@ constexpr int kBarBytes = 512;                      // mbarriers + small shared 
 constexpr int kTileRing = 4;
 constexpr int kTileReaders = 1 + 1 + 1 + kEpiWarps;
 
+// TMEM columns: one 256-column fp32 accumulator, then one set of scale-factor
+// columns per ring stage (4 token + 8 weight columns each), so that a stage's
+// scale copy never targets columns an earlier stage's MMAs may still read.
+// (Two 256-column accumulators plus any scale columns would exceed the 512.)
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kSFCol0 = 256;                   // first scale-factor set
+constexpr uint32_t kSFSetCols = 12;                 // SFA: +0..3, SFB: +4..11
+
 // A kernel variant: the token rows a shared-memory stage holds and the ring
 // depth.  The MMA always reads 128 token rows from a stage's A address; the
 // thin variant keeps only 32 rows per stage, so rows 32..127 of its MMA read
@@ -61,6 +69,7 @@ struct Variant {
   // barriers (2 per stage, 3 accumulator/drain, 2 per tile-ring slot), misc words, votes, tile ring
   static_assert((2 * kStages + 3 + 2 * kTileRing) * 8 + 8 * 4 + 2 * kEpiWarps * 4 + kTileRing * 9 * 4 <= kBarBytes,
                 "barrier region");
+  static_assert(kSFCol0 + kStages * kSFSetCols <= kTmemCols, "scale-factor sets fit TMEM");
   // the MMA's 128-row A window of the last stage stays inside the allocation
   static_assert((kStages - 1) * kABytes + kTileM * kBlockK <= kStages * kStageBytes, "A window");
 };
@@ -68,11 +77,6 @@ using WideVariant = Variant<128, 4, true>;
 using ThinVariant = Variant<32, 6, false>;
 enum VariantId : int { kVariantWide = 0, kVariantThin = 1, kNumVariants = 2 };
 
-// TMEM columns: one 256-column fp32 accumulator, then the scale factors of the
-// stage in flight (two accumulators and the scales would need 524 columns).
-constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kSFACol = 256;                   // 4 columns
-constexpr uint32_t kSFBCol = 260;                   // 8 columns
 
 // ----------------------------------------------------------------- control block
 // 32-bit words at the head of the workspace.

@@ -336,7 +336,6 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
       const uint64_t sfa_desc0 = desc_sf(smem_u32(sSFA));
       const uint64_t sfb_desc0 = desc_sf(smem_u32(sSFB));
       const uint32_t full0 = smem_u32(&full[0]), empty0 = smem_u32(&empty[0]);
-      const uint32_t sfa_t = tmem + kSFACol, sfb_t = tmem + kSFBCol;
       uint32_t stage = 0, phase = 0, aphase = 0, consumed = 0;
       bool ok = true;
       TileFeed feed(s_tiles, tile_full, tile_empty);
@@ -357,6 +356,7 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
           fence_proxy_async_shared();   // scale atoms were written through the generic proxy
           const uint32_t so = stage;
           const uint64_t sfb_d = sfb_desc0 + (uint64_t)(so * (uint32_t)(kSFBBytes >> 4));
+          const uint32_t sfa_t = tmem + kSFCol0 + so * kSFSetCols, sfb_t = sfa_t + 4;
           tc_cp_sf(sfa_t, sfa_desc0 + (uint64_t)(so * (uint32_t)(kSFABytes >> 4)));
           tc_cp_sf(sfb_t, sfb_d);
           if (two_sfb) tc_cp_sf(sfb_t + 4, sfb_d + (512 >> 4));
@@ -469,36 +469,52 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
       vote_buf ^= 1;
       if (!all_ok) break;
       tc_fence_after();
+      // Each thread takes its whole share of the accumulator into registers (one
+      // token row; 64 gate + 64 up columns for L1, up to 128 output columns for
+      // L2), frees the accumulator for the next tile's MMAs, and only then does
+      // the arithmetic and the stores.
       const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16);
       const int row = q * 32 + lane;                       // token row of the block
       const bool valid = row < ti.rows;
       const size_t slot = (size_t)ti.r0 + row;
-      if (q * 32 < ti.rows) {                              // warp-uniform: some row of this quarter is live
+      const bool live_warp = q * 32 < ti.rows;             // warp-uniform: some row of this quarter is live
+      float v[128];
+      const int nh = ti.layer == 1 ? kL1Feat / 2 : ti.n >> 1;   // this warp's columns (per operand for L1)
+      if (live_warp) {
         if (ti.layer == 1) {
-          // ---- L1: 64 of the row's 128 features (blocks 2hh, 2hh+1 of 32): clamp + SwiGLU,
-          // then E4M3 + UE8M0 per 32 features, all in registers
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            tc_ld16(tbase + (uint32_t)(hh * 64 + j * 16), *reinterpret_cast<float(*)[16]>(&v[j * 16]));
+            tc_ld16(tbase + (uint32_t)(kL1Feat + hh * 64 + j * 16), *reinterpret_cast<float(*)[16]>(&v[64 + j * 16]));
+          }
+        } else {
+          const int c_beg = hh * nh;
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            if (j * 16 < nh) tc_ld16(tbase + (uint32_t)(c_beg + j * 16), *reinterpret_cast<float(*)[16]>(&v[j * 16]));
+        }
+        tc_wait_ld();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(tempty));
+      if (live_warp) {
+        if (ti.layer == 1) {
+          // ---- L1: features [64hh, 64hh + 64) of the row: clamp + SwiGLU, then E4M3 + UE8M0 per 32
           const float L = p.clamp;
-          uint8_t* dst = l1a + slot * p.I + ti.nb * kL1Feat;
+          uint8_t* dst = l1a + slot * p.I + ti.nb * kL1Feat + hh * 64;
           uint32_t sfw = 0;
-#pragma unroll 1
+#pragma unroll
           for (int bi = 0; bi < 2; ++bi) {
-            const int blk = 2 * hh + bi;
-            float h[32];
+            float* h = &v[bi * 32];                          // SwiGLU result overwrites the gate values
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-              float g[16], u[16];
-              tc_ld16(tbase + (uint32_t)(blk * 32 + half * 16), g);
-              tc_ld16(tbase + (uint32_t)(kL1Feat + blk * 32 + half * 16), u);
-              tc_wait_ld();
-#pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                float gg = g[i], uu = u[i];
-                if (p.use_clamp) {
-                  gg = fminf(gg, L);
-                  uu = fminf(fmaxf(uu, -L), L);
-                }
-                h[half * 16 + i] = gg * __fdividef(1.0f, 1.0f + __expf(-gg)) * uu;   // fast-math SiLU
+            for (int i = 0; i < 32; ++i) {
+              float gg = v[bi * 32 + i], uu = v[64 + bi * 32 + i];
+              if (p.use_clamp) {
+                gg = fminf(gg, L);
+                uu = fminf(fmaxf(uu, -L), L);
               }
+              h[i] = gg * __fdividef(1.0f, 1.0f + __expf(-gg)) * uu;   // fast-math SiLU
             }
             float a = 0.f;
 #pragma unroll
@@ -511,7 +527,7 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
               w[i] = e4m3_code(h[4 * i] * inv) | (e4m3_code(h[4 * i + 1] * inv) << 8) |
                      (e4m3_code(h[4 * i + 2] * inv) << 16) | (e4m3_code(h[4 * i + 3] * inv) << 24);
             if (valid) {
-              uint4* d4 = reinterpret_cast<uint4*>(dst + blk * 32);
+              uint4* d4 = reinterpret_cast<uint4*>(dst + bi * 32);
               d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
               d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
             }
@@ -521,14 +537,13 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
             *reinterpret_cast<uint16_t*>(l1a_sf + slot * (p.I / 32) + ti.nb * (kL1Feat / 32) + 2 * hh) =
                 (uint16_t)sfw;
         } else {
-          // ---- L2: half of the row's N hidden outputs x top-k weight -> fp32 row of the flat assignment
+          // ---- L2: this warp's nh output columns x top-k weight -> fp32 row of the flat assignment
           int f = 0;
           float wt = 0.f;
           if (valid) {
             f = __ldg(perm + slot);
             wt = __ldg(p.topk_w + f);
           }
-          const int nh = ti.n >> 1;
           const int c_beg = hh * nh;
           if constexpr (V::kXpose) {
             // 16 columns at a time pass through this warp's transpose buffer (32 rows x four
@@ -537,59 +552,44 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
             // then stores chunk l % 4 of rows l / 4 + 8i, whole 64-byte row segments.
             float4* xb = reinterpret_cast<float4*>(sX + ew * (32 * 16));
             const int rr = lane >> 2, cc = lane & 3;
-            float* dst[4];
-            bool live[4];
+            int fr[4];
+            uint32_t live = 0;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               const int r = rr + 8 * i;
-              const int fr = __shfl_sync(0xffffffffu, f, r);
-              live[i] = q * 32 + r < ti.rows;
-              dst[i] = stage_out + (size_t)fr * p.H + ti.nb * kTileN + 4 * cc;
+              fr[i] = __shfl_sync(0xffffffffu, f, r);
+              live |= (q * 32 + r < ti.rows ? 1u : 0u) << i;
             }
+            float* const col0 = stage_out + ti.nb * kTileN + c_beg + 4 * cc;
             const int wsw = (lane >> 1) & 3;
-#pragma unroll 1
-            for (int c0 = c_beg; c0 < c_beg + nh; c0 += 16) {
-              float v[16];
-              tc_ld16(tbase + (uint32_t)c0, v);
-              tc_wait_ld();
 #pragma unroll
-              for (int j = 0; j < 4; ++j)
-                xb[lane * 4 + (j ^ wsw)] =
-                    make_float4(v[4 * j] * wt, v[4 * j + 1] * wt, v[4 * j + 2] * wt, v[4 * j + 3] * wt);
-              __syncwarp();
+            for (int j = 0; j < 8; ++j) {
+              if (j * 16 < nh) {
 #pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                const int r = rr + 8 * i;
-                const float4 val = xb[r * 4 + (cc ^ ((r >> 1) & 3))];
-                if (live[i]) *reinterpret_cast<float4*>(dst[i] + c0) = val;
+                for (int t = 0; t < 4; ++t)
+                  xb[lane * 4 + (t ^ wsw)] = make_float4(v[j * 16 + 4 * t] * wt, v[j * 16 + 4 * t + 1] * wt,
+                                                         v[j * 16 + 4 * t + 2] * wt, v[j * 16 + 4 * t + 3] * wt);
+                __syncwarp();
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  const int r = rr + 8 * i;
+                  const float4 val = xb[r * 4 + (cc ^ ((r >> 1) & 3))];
+                  if ((live >> i) & 1u) *reinterpret_cast<float4*>(col0 + (size_t)fr[i] * p.H + j * 16) = val;
+                }
+                __syncwarp();
               }
-              __syncwarp();
             }
           } else {
             // few rows per tile: each thread stores its own row directly
-            float* dst = stage_out + (size_t)f * p.H + ti.nb * kTileN;
-#pragma unroll 1
-            for (int c0 = c_beg; c0 < c_beg + nh; c0 += 32) {
-              float v[16], v2[16];
-              tc_ld16(tbase + (uint32_t)c0, v);
-              tc_ld16(tbase + (uint32_t)(c0 + 16), v2);
-              tc_wait_ld();
-              if (valid) {
-                float4* d4 = reinterpret_cast<float4*>(dst + c0);
+            float4* d4 = reinterpret_cast<float4*>(stage_out + (size_t)f * p.H + ti.nb * kTileN + c_beg);
+            if (valid) {
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                  d4[i] = make_float4(v[4 * i] * wt, v[4 * i + 1] * wt, v[4 * i + 2] * wt, v[4 * i + 3] * wt);
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                  d4[4 + i] = make_float4(v2[4 * i] * wt, v2[4 * i + 1] * wt, v2[4 * i + 2] * wt, v2[4 * i + 3] * wt);
-              }
+              for (int j = 0; j < 32; ++j)
+                if (j * 4 < nh) d4[j] = make_float4(v[4 * j] * wt, v[4 * j + 1] * wt, v[4 * j + 2] * wt, v[4 * j + 3] * wt);
             }
           }
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(tempty));
       if (ti.layer == 1) {
         fence_proxy_async_global();
         __threadfence();
