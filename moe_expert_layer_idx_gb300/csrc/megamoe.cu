@@ -161,9 +161,6 @@ __device__ __forceinline__ uint16_t bf16_bits_rn(float v) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(v));
 }
 
-__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" :: "r"(bar) : "memory");
-}
 
 template <class V>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -181,7 +178,7 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
   uint8_t* sSFB = sSFA + kStages * kSFABytes;         // [kStages] two weight scale atoms
   float* sX = reinterpret_cast<float*>(sSFB + kStages * kSFBBytes);   // [kEpiWarps] transpose buffers
   uint64_t* bars = reinterpret_cast<uint64_t*>(sSFB + kStages * kSFBBytes + V::kXposeBytes);
-  uint64_t* full = bars;                     // [kStages] TMA bytes + 32 scale-loader lanes' cp.async landed
+  uint64_t* full = bars;                     // [kStages] both producers' TMA bytes + the scale loader's atoms
   uint64_t* empty = bars + kStages;          // [kStages] MMAs reading the stage are done
   uint64_t* tfull = bars + 2 * kStages;      // accumulator ready
   uint64_t* tempty = tfull + 1;              // accumulator drained (every epilogue warp)
@@ -213,7 +210,7 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 2 + 32);
+      mbar_init(&full[s], 2 + 1);
       mbar_init(&empty[s], 1);
     }
     mbar_init(tfull, 1);
@@ -352,8 +349,6 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
         const bool two_sfb = ti.n > 128;
         for (int kb = 0; kb < ti.ks; ++kb) {
           if (!mbar_wait(full0 + stage * 8u, phase, ctrl, to, (kSiteFull << 24) | tag)) { ok = false; break; }
-          tc_fence_after();
-          fence_proxy_async_shared();   // scale atoms were written through the generic proxy
           const uint32_t so = stage;
           const uint64_t sfb_d = sfb_desc0 + (uint64_t)(so * (uint32_t)(kSFBBytes >> 4));
           const uint32_t sfa_t = tmem + kSFCol0 + so * kSFSetCols, sfb_t = sfa_t + 4;
@@ -380,7 +375,24 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
     }
   } else if (warp == 2) {
     // ---------------- scale loader (32 lanes)
-    uint32_t stage = 0, phase = 0, armed = 0;
+    // Each stage's UE8M0 bytes are gathered with cp.async (one commit group per
+    // stage).  The tensor core reads the atoms through the async proxy, so a
+    // stage is released only after its copies have landed and every lane has
+    // fenced them: lane 0 then arrives on the stage's full barrier.  The
+    // release trails the issue by kSfLag stages (<= the ring depth, so the
+    // ring always drains), which keeps the copies' latency off the loop; the
+    // held-back stages are released before any wait on another tile's progress.
+    constexpr uint32_t kSfLag = 2;
+    static_assert(kSfLag <= (uint32_t)kStages, "release lag");
+    uint32_t stage = 0, phase = 0, armed = 0, gathered = 0, astage = 0;
+    auto release_oldest = [&](bool all) {
+      if (all) cp_async_wait<0>(); else cp_async_wait<kSfLag - 1>();
+      fence_proxy_async_shared();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&full[astage]));
+      ++armed;
+      if (++astage == (uint32_t)kStages) astage = 0;
+    };
     int ready_key = -1;
     const int H32 = p.H / 32, I32 = p.I / 32;
     TileFeed feed(s_tiles, tile_full, tile_empty);
@@ -392,6 +404,8 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
       bool ok = true;
       const int key = ti.e * 2 + ti.layer - 1;
       if (key != ready_key) {
+        // The dependency may wait on tiles whose MMAs need the stages still held back: release them first.
+        while (armed < gathered) release_oldest(true);
         if (lane == 0) {
           ok = (ti.layer == 1)
                    ? counter_wait(&arrival[ti.e], (uint32_t)__ldg(counts + ti.e), ctrl, to, (kSiteArrival << 24) | tag)
@@ -434,13 +448,14 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
           for (int j = 0; j < 4; ++j)
             cp_async_4(dB + 512 + j * 4, b_sf_base + (size_t)(b_row1 + lane + 32 * j) * kstride + kb * 4);
         }
-        cp_async_mbar_arrive_noinc(smem_u32(&full[stage]));
-        ++armed;
+        cp_async_commit();
+        ++gathered;
+        if (gathered - armed == kSfLag) release_oldest(false);
         if (++stage == kStages) { stage = 0; phase ^= 1u; }
       }
       if (!ok) break;
     }
-    cp_async_wait<0>();
+    while (armed < gathered) release_oldest(true);
     if (lane == 0) s_misc[4] = armed;
   } else {
     // ---------------- epilogue: warp w reads TMEM lanes 32q..32q+31 (token rows), q = w % 4;
@@ -606,15 +621,14 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
   if (threadIdx.x == 0) {
     // After an abort, TMA loads may still be landing.  Each issued but
     // unconsumed stage's barrier completes once its bytes land, provided the
-    // scale loader's 32 arrivals and both producers' arrivals were made; make
-    // the missing ones here (a role that stopped early: its arrival, no
-    // bytes; the scale loader has already waited for its own copies).
+    // scale loader's and both producers' arrivals were made; make the missing
+    // ones here (a role that stopped early: its arrival, no bytes; the scale
+    // loader has already waited for its own copies).
     const uint32_t issued0 = s_misc[2], issued1 = s_misc[5], consumed = s_misc[1], armed = s_misc[4];
     const uint32_t issued = issued0 > issued1 ? issued0 : issued1;
     for (uint32_t s = consumed; s < issued; ++s) {
       const uint32_t bar = smem_u32(&full[s % kStages]);
-      if (s >= armed)
-        for (int i = 0; i < 32; ++i) mbar_arrive(bar);
+      if (s >= armed) mbar_arrive(bar);
       if (s >= issued0) mbar_arrive(bar);
       if (s >= issued1) mbar_arrive(bar);
       if (!mbar_wait_drain(bar, (s / kStages) & 1u, to)) set_error(ctrl, MM_ERR_TIMEOUT, kSiteDrain << 24);
