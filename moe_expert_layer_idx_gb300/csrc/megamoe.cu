@@ -249,7 +249,15 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
       const int e = __ldg(p.topk_idx + f);
       const uint4* src = reinterpret_cast<const uint4*>(p.x + (size_t)t * H);
       uint4* dst = reinterpret_cast<uint4*>(xs + (size_t)s * H);
-      for (int c = lane; c < nvec; c += 32) dst[c] = __ldg(src + c);
+      for (int c0 = lane; c0 < nvec; c0 += 32 * 8) {       // 8 independent loads in flight per lane
+        uint4 v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if (c0 + 32 * i < nvec) v[i] = __ldg(src + c0 + 32 * i);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if (c0 + 32 * i < nvec) dst[c0 + 32 * i] = v[i];
+      }
       const uint32_t* ssf = reinterpret_cast<const uint32_t*>(p.x_sf + (size_t)t * (H / 32));
       uint32_t* dsf = reinterpret_cast<uint32_t*>(xs_sf + (size_t)s * (H / 32));
       for (int c = lane; c < nsf; c += 32) dsf[c] = __ldg(ssf + c);
@@ -670,12 +678,23 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
       float acc[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-      for (int j = 0; j < k; ++j) {
-        if (!((valid >> j) & 1u)) continue;
-        const float4 a = __ldcg(rows + (size_t)j * (H / 4) + 2 * c);
-        const float4 b = __ldcg(rows + (size_t)j * (H / 4) + 2 * c + 1);
-        acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
-        acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+      // the k rows' loads go out together (8 at a time), then the sum runs in ascending j
+      for (int j0 = 0; j0 < k; j0 += 8) {
+        float4 a[8], b[8];
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+          if (j0 + jj < k) {
+            a[jj] = __ldcg(rows + (size_t)(j0 + jj) * (H / 4) + 2 * c);
+            b[jj] = __ldcg(rows + (size_t)(j0 + jj) * (H / 4) + 2 * c + 1);
+          }
+        }
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+          if (j0 + jj < k && ((valid >> (j0 + jj)) & 1u)) {
+            acc[0] += a[jj].x; acc[1] += a[jj].y; acc[2] += a[jj].z; acc[3] += a[jj].w;
+            acc[4] += b[jj].x; acc[5] += b[jj].y; acc[6] += b[jj].z; acc[7] += b[jj].w;
+          }
+        }
       }
       uint32_t o[4];
 #pragma unroll
