@@ -1,6 +1,6 @@
 """The fused layer on the GPU against the fp64 oracle, on shapes the oracle
 finishes in seconds that still span several L1/L2 tiles, split experts into
-several N blocks and leave ragged tails."""
+several token blocks, leave ragged tails and exercise both kernel variants."""
 import numpy as np
 import pytest
 import torch
@@ -15,16 +15,22 @@ from layer_inputs import (ExpertCache, GpuTokens, GpuWeights, bf16_to_np, close_
 pytestmark = pytest.mark.gpu
 
 SMALL = {
+    # thin variant (<= 16 assignments per expert on average: 32-row token stages)
     "tiny": synth.CONFIGS["tiny"],
-    # ~267 assignments per expert: two N blocks each, 3 L2 tiles, 4 L1 tiles
+    # wide variant: ~267 assignments per expert -> 3 token blocks (one of them a full
+    # 128-row block, loaded as one 128-row box), L2 tail of 128 hidden rows (H = 384)
     "ragged": synth.Config("ragged", T=400, H=384, I=256, E=3, k=2, clamp=7.0, seed=1),
     # many experts with 0-3 tokens, some slots empty, no clamp
     "sparse": synth.Config("sparse", T=37, H=256, I=128, E=16, k=4, clamp=0.0, seed=2),
-    # skewed routing, wider hidden, I/64 = 6 L1 tiles per expert
+    # skewed routing (hot experts split into several 32-row blocks), 4 L2 / 3 L1 weight blocks
     "wide": synth.Config("wide", T=129, H=1024, I=384, E=96, k=8, clamp=10.0, skew=True, seed=3),
-    # ~6 tokens per expert (the deep-ring variant for decode-sized batches), and a
-    # hot expert split into several N blocks
+    # ~6 tokens per expert, a hot expert split into several blocks
     "thin": synth.Config("thin", T=100, H=512, I=256, E=64, k=4, clamp=7.0, skew=True, seed=5),
+    # thin variant with the 128-row L2 tail (H = 384)
+    "thin_tail": synth.Config("thin_tail", T=48, H=384, I=128, E=8, k=2, clamp=7.0, seed=6),
+    # wide variant, one ~75-token block per expert: five 16-row token boxes split 3/2
+    # between the two producers
+    "odd_boxes": synth.Config("odd_boxes", T=150, H=256, I=128, E=2, k=1, clamp=7.0, seed=7),
 }
 
 
