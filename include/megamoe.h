@@ -131,6 +131,28 @@ int mm_forward(int num_tokens, int experts, int topk, int hidden, int inter,
                void* workspace, size_t workspace_bytes, mm_stream_t stream);
 
 /*
+ * mm_forward_bf16 -- mm_forward on bfloat16 activations: the quantisation
+ * that precedes the fused call in the pages' pipeline ([P1] Fix, the
+ * "pre-dispatch" step; [P2] 关键源码片段, the quantisation done before
+ * fp8_fp4_mega_moe) is folded into the layer's dispatch.
+ *
+ *   x_bf16    bfloat16              [T, H]        16-byte aligned
+ *
+ * Every other argument, the workspace and the error behaviour are those of
+ * mm_forward.  Each token's row is read once; every 32-element block is
+ * quantised to E4M3 with one UE8M0 scale by the same rule as mm_quantize_mx
+ * (the smallest power of two 2^s with max|v| <= 448 * 2^s, s in [-127, 127];
+ * elements round to nearest even, saturating) and written to each of the
+ * token's expert slots.  The result equals mm_forward on mm_quantize_mx of
+ * the same values, bit for bit.
+ */
+int mm_forward_bf16(int num_tokens, int experts, int topk, int hidden, int inter,
+                    const void* x_bf16, const int32_t* topk_idx, const float* topk_w,
+                    const void* l1_w, const void* l1_sf, const void* l2_w, const void* l2_sf,
+                    void* y, float clamp, int num_sms,
+                    void* workspace, size_t workspace_bytes, mm_stream_t stream);
+
+/*
  * mm_set_reserved_sms -- SMs left free for other streams by every launch
  * ([P1] Summary: two by default; [P2] 实现拆解 item 1: 0 disables it).
  * n < 0 is taken as 0.  Process-wide; read at each launch.  Returns the

@@ -50,6 +50,7 @@ _SIGS = {
     "mm_workspace_region": (_c_int, [_c_int] * 6 + [_c_vp, _c_vp]),
     "mm_quantize_mx": (_c_int, [_c_vp, _c_ll, _c_ll, _c_int, _c_vp, _c_vp, _c_vp]),
     "mm_forward_noalloc": (_c_int, [_c_int] * 5 + [_c_vp] * 9 + [ctypes.c_float, _c_int, _c_vp]),
+    "mm_forward_bf16": (_c_int, [_c_int] * 5 + [_c_vp] * 8 + [ctypes.c_float, _c_int, _c_vp, _c_size, _c_vp]),
 }
 
 
@@ -104,6 +105,16 @@ def mm_forward(num_tokens, experts, topk, hidden, inter, x, x_sf, topk_idx, topk
     return lib().mm_forward(num_tokens, experts, topk, hidden, inter, _ptr(x), _ptr(x_sf), _ptr(topk_idx),
                             _ptr(topk_w), _ptr(l1_w), _ptr(l1_sf), _ptr(l2_w), _ptr(l2_sf), _ptr(y),
                             float(clamp), num_sms, _ptr(workspace), workspace_bytes, _stream(stream))
+
+
+def mm_forward_bf16(num_tokens, experts, topk, hidden, inter, x_bf16, topk_idx, topk_w, l1_w, l1_sf,
+                    l2_w, l2_sf, y, clamp, num_sms, workspace, workspace_bytes=None, stream=None) -> int:
+    """mm_forward on bf16 activations [T, H], quantised to E4M3 + UE8M0/32 in the layer's dispatch."""
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    return lib().mm_forward_bf16(num_tokens, experts, topk, hidden, inter, _ptr(x_bf16), _ptr(topk_idx),
+                                 _ptr(topk_w), _ptr(l1_w), _ptr(l1_sf), _ptr(l2_w), _ptr(l2_sf), _ptr(y),
+                                 float(clamp), num_sms, _ptr(workspace), workspace_bytes, _stream(stream))
 
 
 def mm_set_reserved_sms(n) -> int:

@@ -184,18 +184,24 @@ int mm_grid_size(int device_sms, int reserved_sms, int num_sms, int max_resident
 void mm_set_wait_timeout_ns(unsigned long long ns) { g_timeout_ns.store(ns ? ns : kDefaultTimeoutNs); }
 unsigned long long mm_get_wait_timeout_ns(void) { return g_timeout_ns.load(); }
 
-int mm_forward(int num_tokens, int experts, int topk, int hidden, int inter,
-               const void* x, const void* x_sf, const int32_t* topk_idx, const float* topk_w,
-               const void* l1_w, const void* l1_sf, const void* l2_w, const void* l2_sf,
-               void* y, float clamp, int num_sms,
-               void* workspace, size_t workspace_bytes, mm_stream_t stream) {
+// The fused layer on E4M3 activations (x, x_sf) when x_bf16 is null, else on
+// bf16 activations quantised in the dispatch.  A missing input of either kind
+// is MM_ERR_INVALID_ARG (after the shape checks and the T = 0 early return).
+static int forward_impl(int num_tokens, int experts, int topk, int hidden, int inter,
+                        const void* x, const void* x_sf, const void* x_bf16, const int32_t* topk_idx,
+                        const float* topk_w, const void* l1_w, const void* l1_sf, const void* l2_w,
+                        const void* l2_sf, void* y, float clamp, int num_sms,
+                        void* workspace, size_t workspace_bytes, mm_stream_t stream) {
   const int T = num_tokens, E = experts, k = topk, H = hidden, I = inter;
   int rc = check_shape(T, E, k, H, I);
   if (rc != MM_OK) return rc;
   if (T == 0) return MM_OK;
-  if (!x || !x_sf || !topk_idx || !topk_w || !l1_w || !l1_sf || !l2_w || !l2_sf || !y) return MM_ERR_INVALID_ARG;
-  if (!aligned(x, 16) || !aligned(x_sf, 4) || !aligned(topk_idx, 4) || !aligned(topk_w, 4) ||
-      !aligned(l1_w, 32) || !aligned(l1_sf, 4) || !aligned(l2_w, 32) || !aligned(l2_sf, 4) || !aligned(y, 16))
+  const bool fp8_in = x_bf16 == nullptr;
+  if ((fp8_in && (!x || !x_sf)) || !topk_idx || !topk_w || !l1_w || !l1_sf || !l2_w || !l2_sf || !y)
+    return MM_ERR_INVALID_ARG;
+  if ((fp8_in && (!aligned(x, 16) || !aligned(x_sf, 4))) || (!fp8_in && !aligned(x_bf16, 16)) ||
+      !aligned(topk_idx, 4) || !aligned(topk_w, 4) || !aligned(l1_w, 32) || !aligned(l1_sf, 4) ||
+      !aligned(l2_w, 32) || !aligned(l2_sf, 4) || !aligned(y, 16))
     return MM_ERR_INVALID_ARG;
   if (std::isnan(clamp)) return MM_ERR_INVALID_ARG;
   Layout L;
@@ -239,8 +245,9 @@ int mm_forward(int num_tokens, int experts, int topk, int hidden, int inter,
   fp.clamp = fp.use_clamp ? clamp : 0.f;
   fp.a_box128 = A >= kTileM ? 1 : 0;
   fp.timeout_ns = g_timeout_ns.load();
-  fp.x = static_cast<const uint8_t*>(x);
-  fp.x_sf = static_cast<const uint8_t*>(x_sf);
+  fp.x = fp8_in ? static_cast<const uint8_t*>(x) : nullptr;
+  fp.x_sf = fp8_in ? static_cast<const uint8_t*>(x_sf) : nullptr;
+  fp.x_bf16 = fp8_in ? nullptr : static_cast<const uint16_t*>(x_bf16);
   fp.topk_idx = topk_idx;
   fp.topk_w = topk_w;
   fp.w1_sf = static_cast<const uint8_t*>(l1_sf);
@@ -250,6 +257,24 @@ int mm_forward(int num_tokens, int experts, int topk, int hidden, int inter,
   fp.L = L;
   if (layer_launch(variant, grid, s, maps, fp) != cudaSuccess) return MM_ERR_CUDA;
   return MM_OK;
+}
+
+int mm_forward(int num_tokens, int experts, int topk, int hidden, int inter,
+               const void* x, const void* x_sf, const int32_t* topk_idx, const float* topk_w,
+               const void* l1_w, const void* l1_sf, const void* l2_w, const void* l2_sf,
+               void* y, float clamp, int num_sms,
+               void* workspace, size_t workspace_bytes, mm_stream_t stream) {
+  return forward_impl(num_tokens, experts, topk, hidden, inter, x, x_sf, nullptr, topk_idx, topk_w, l1_w, l1_sf,
+                      l2_w, l2_sf, y, clamp, num_sms, workspace, workspace_bytes, stream);
+}
+
+int mm_forward_bf16(int num_tokens, int experts, int topk, int hidden, int inter,
+                    const void* x_bf16, const int32_t* topk_idx, const float* topk_w,
+                    const void* l1_w, const void* l1_sf, const void* l2_w, const void* l2_sf,
+                    void* y, float clamp, int num_sms,
+                    void* workspace, size_t workspace_bytes, mm_stream_t stream) {
+  return forward_impl(num_tokens, experts, topk, hidden, inter, nullptr, nullptr, x_bf16, topk_idx, topk_w, l1_w,
+                      l1_sf, l2_w, l2_sf, y, clamp, num_sms, workspace, workspace_bytes, stream);
 }
 
 int mm_route(int num_tokens, int experts, int topk, int hidden, int inter, const int32_t* topk_idx,

@@ -134,8 +134,9 @@ struct ForwardParams {
   float clamp;
   int a_box128;                // token count allows one 128-row TMA box per stage
   unsigned long long timeout_ns;
-  const uint8_t* x;
+  const uint8_t* x;            // E4M3 activations and scales, or
   const uint8_t* x_sf;
+  const uint16_t* x_bf16;      // bf16 activations, quantised in the dispatch (then x, x_sf are null)
   const int32_t* topk_idx;
   const float* topk_w;
   const uint8_t* w1_sf;

@@ -239,7 +239,61 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
   const uint32_t tmem = s_misc[0];
 
   // ------------------------------------------------------------ 0. dispatch
-  {
+  if (p.x_bf16 != nullptr) {
+    // bf16 activations: one warp per token reads its row once; lane b quantises
+    // 32-element blocks b, b + 32, ... (E4M3 + UE8M0 by the scale rule of the
+    // L1 epilogue) and writes each block to every slot of the token, then each
+    // slot's expert arrival count is released.
+    const int32_t* inv = reinterpret_cast<const int32_t*>(p.ws + p.L.inv);
+    const int H = p.H, k = p.k, nblk = H / 32;
+    for (int t = blockIdx.x * (kThreads / 32) + warp; t < p.T; t += gridDim.x * (kThreads / 32)) {
+      int my_e = -1, my_slot = -1;                   // lane j < k: slot j of the token
+      if (lane < k) {
+        my_e = __ldg(p.topk_idx + (size_t)t * k + lane);
+        if (my_e >= 0) my_slot = __ldg(inv + (size_t)t * k + lane);
+      }
+      int slots[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) slots[j] = __shfl_sync(0xffffffffu, my_slot, j);
+      const uint4* src = reinterpret_cast<const uint4*>(p.x_bf16 + (size_t)t * H);
+      for (int b = lane; b < nblk; b += 32) {
+        float v[32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint4 q = __ldg(src + 4 * b + c);
+          const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            v[8 * c + 2 * i] = __uint_as_float(w[i] << 16);             // bf16 -> fp32 is exact
+            v[8 * c + 2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+          }
+        }
+        float a = 0.f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) a = fmaxf(a, fabsf(v[i]));
+        const int sc = block_scale_exp<true>(a);
+        const float inv_s = exp2_neg(sc);
+        uint32_t w[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          w[i] = e4m3_code(v[4 * i] * inv_s) | (e4m3_code(v[4 * i + 1] * inv_s) << 8) |
+                 (e4m3_code(v[4 * i + 2] * inv_s) << 16) | (e4m3_code(v[4 * i + 3] * inv_s) << 24);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          if (j < k && slots[j] >= 0) {
+            uint4* d4 = reinterpret_cast<uint4*>(xs + (size_t)slots[j] * H + 32 * b);
+            d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+            xs_sf[(size_t)slots[j] * nblk + b] = (uint8_t)(sc + 127);
+          }
+        }
+      }
+      fence_proxy_async_global();
+      __threadfence();
+      __syncwarp();
+      if (my_e >= 0) red_release_add(&arrival[my_e], 1u);
+    }
+  } else {
     const int nvalid = __ldg(offsets + p.E);
     const int H = p.H;
     const int nvec = H / 16, nsf = H / 128;

@@ -153,6 +153,24 @@ def test_forward_argument_errors(lib):
     assert _fwd(workspace_bytes=need - 1) == mm.MM_ERR_WORKSPACE_TOO_SMALL
 
 
+def _fwd_bf16(**kw):
+    a = dict(num_tokens=64, experts=8, topk=2, hidden=256, inter=128, x_bf16=FAKE, topk_idx=FAKE,
+             topk_w=FAKE, l1_w=FAKE, l1_sf=FAKE, l2_w=FAKE, l2_sf=FAKE, y=FAKE, clamp=7.0, num_sms=0,
+             workspace=FAKE, workspace_bytes=1 << 40, stream=0)
+    a.update(kw)
+    return mm.mm_forward_bf16(**a)
+
+
+def test_forward_bf16_argument_errors(lib):
+    assert _fwd_bf16(num_tokens=0) == mm.MM_OK
+    assert _fwd_bf16(hidden=200) == mm.MM_ERR_UNSUPPORTED_SHAPE
+    assert _fwd_bf16(x_bf16=0) == mm.MM_ERR_INVALID_ARG            # no activations of either kind
+    assert _fwd_bf16(x_bf16=FAKE + 8) == mm.MM_ERR_INVALID_ARG     # bf16 rows need 16-byte alignment
+    assert _fwd_bf16(topk_w=0) == mm.MM_ERR_INVALID_ARG
+    need = mm.mm_workspace_size(64, 8, 2, 256, 128)
+    assert _fwd_bf16(workspace_bytes=need - 1) == mm.MM_ERR_WORKSPACE_TOO_SMALL
+
+
 def test_route_and_quantize_argument_errors(lib):
     assert mm.mm_route(64, 8, 2, 256, 128, FAKE, FAKE, 10, 0) == mm.MM_ERR_WORKSPACE_TOO_SMALL
     assert mm.mm_route(64, 8, 2, 256, 128, 0, FAKE, 1 << 40, 0) == mm.MM_ERR_INVALID_ARG
@@ -166,3 +184,4 @@ def test_forward_without_device(lib):
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     assert _fwd() == mm.MM_ERR_NO_DEVICE
+    assert _fwd_bf16() == mm.MM_ERR_NO_DEVICE
