@@ -243,6 +243,19 @@ def run_ours(args, rank, world, local_rank):
 
     tokens_per_s, ms = replica_throughput(ev0.elapsed_time(ev1) / args.steps, T, world, max_over_ranks)
 
+    # ---- per-step distribution (separately, each step between its own events)
+    n_pct = max(1, min(args.steps, 100))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_pct)]
+    for a_, b_ in evs:
+        a_.record(stream)
+        step()
+        b_.record(stream)
+    torch.cuda.synchronize(dev)
+    per_step = sorted(a_.elapsed_time(b_) for a_, b_ in evs)
+    pct = {"p10": round(float(np.percentile(per_step, 10)), 4), "p50": round(float(np.percentile(per_step, 50)), 4),
+           "p90": round(float(np.percentile(per_step, 90)), 4), "steps": n_pct}
+    check_status()
+
     # ---- routing kernel alone (to isolate the persistent layer kernel's time)
     ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ea.record(stream)
@@ -311,7 +324,7 @@ def run_ours(args, rank, world, local_rank):
         "tokens_per_s": tokens_per_s, "ms": ms, "route_ms": route_ms, "roofline": roofline,
         "e2e": {"value": round(e2e_tps, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
-        "clocks": clk.summary(), "wall_s": t_wall, "gpu_launches": 2 * args.steps,
+        "clocks": clk.summary(), "wall_s": t_wall, "gpu_launches": 2 * args.steps, "step_ms": pct,
         "cfg": cfg, "touched": touched,
     }
 
@@ -421,7 +434,7 @@ def main():
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3xe2m1->f32",
             "data": "synthetic", "config": config, "roofline": res["roofline"], "cpu_baseline": cpu,
             "e2e": res["e2e"], "gpu_launches": res["gpu_launches"], "clocks": res["clocks"],
-            "route_ms": round(res["route_ms"], 4)}
+            "route_ms": round(res["route_ms"], 4), "step_ms_percentiles": res["step_ms"]}
     print(json.dumps(line), flush=True)
     return 0
 

@@ -18,9 +18,12 @@ What it computes (the single-GPU fused MegaMoE expert layer):
 * ``moe``      -- the layer: L1 gate/up GEMM, clamp, SwiGLU, FP8 requantisation
   of the L1 activations, L2 down GEMM, and the top-k weighted combine into a
   bf16 output, accumulated in fp64.
+* ``moe_bf16`` -- the bf16 x bf16 variant of the layer (the BF16 MegaMoE kernel
+  that DeepGEMM PR #451 fixes beside the FP8/FP4 one): the same steps with
+  bfloat16 inputs, weights and L1 activations instead of the FP8/FP4 codes.
 
 Every function is pinned by CPU tests (``tests/test_oracle_*.py``) against
 closed forms, library routines, brute force and exact rational arithmetic;
 none is "parity unpinned".
 """
-from . import formats, routing, moe  # noqa: F401
+from . import formats, routing, moe, moe_bf16  # noqa: F401
