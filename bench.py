@@ -169,38 +169,58 @@ def run_ours(args, rank, world, local_rank):
         if rc != mm.MM_OK:
             raise RuntimeError(f"mm_quantize_mx: {mm.STATUS_NAMES.get(rc, rc)}")
 
-    l1_w = torch.empty(E, 2 * I, H // 2, dtype=torch.uint8, device=dev)
-    l1_sf = torch.empty(E, 2 * I, H // 32, dtype=torch.uint8, device=dev)
-    l2_w = torch.empty(E, H, I // 2, dtype=torch.uint8, device=dev)
-    l2_sf = torch.empty(E, H, I // 32, dtype=torch.uint8, device=dev)
+    bf16_layer = args.layer == "bf16"
+    if bf16_layer:
+        # the bf16 x bf16 layer: the same seeded values, rounded to bf16
+        l1_w = torch.empty(E, 2 * I, H, dtype=torch.bfloat16, device=dev)
+        l2_w = torch.empty(E, H, I, dtype=torch.bfloat16, device=dev)
+        l1_sf = l2_sf = x_sf = None
+    else:
+        l1_w = torch.empty(E, 2 * I, H // 2, dtype=torch.uint8, device=dev)
+        l1_sf = torch.empty(E, 2 * I, H // 32, dtype=torch.uint8, device=dev)
+        l2_w = torch.empty(E, H, I // 2, dtype=torch.uint8, device=dev)
+        l2_sf = torch.empty(E, H, I // 32, dtype=torch.uint8, device=dev)
     chunk = 16
     buf = torch.empty(min(chunk, E) * 2 * I * H, dtype=torch.float32, device=dev)
     for e0 in range(0, E, chunk):
         e1 = min(E, e0 + chunk)
         n1, n2 = (e1 - e0) * 2 * I * H, (e1 - e0) * H * I
         synth.normal_f32_cuda(cfg.seed, synth.TENSOR_W1, e0 * 2 * I * H, buf[:n1], synth.weight_scale(H))
-        quant(buf[:n1], (e1 - e0) * 2 * I, H, mm.MM_FMT_E2M1, l1_w[e0:e1], l1_sf[e0:e1])
+        if bf16_layer:
+            l1_w[e0:e1].copy_(buf[:n1].view(e1 - e0, 2 * I, H))
+        else:
+            quant(buf[:n1], (e1 - e0) * 2 * I, H, mm.MM_FMT_E2M1, l1_w[e0:e1], l1_sf[e0:e1])
         synth.normal_f32_cuda(cfg.seed, synth.TENSOR_W2, e0 * H * I, buf[:n2], synth.weight_scale(I))
-        quant(buf[:n2], (e1 - e0) * H, I, mm.MM_FMT_E2M1, l2_w[e0:e1], l2_sf[e0:e1])
+        if bf16_layer:
+            l2_w[e0:e1].copy_(buf[:n2].view(e1 - e0, H, I))
+        else:
+            quant(buf[:n2], (e1 - e0) * H, I, mm.MM_FMT_E2M1, l2_w[e0:e1], l2_sf[e0:e1])
     del buf
     xf = torch.empty(T * H, dtype=torch.float32, device=dev)
     synth.normal_f32_cuda(seed, synth.TENSOR_X, 0, xf)
-    x = torch.empty(T, H, dtype=torch.uint8, device=dev)
-    x_sf = torch.empty(T, H // 32, dtype=torch.uint8, device=dev)
-    quant(xf, T, H, mm.MM_FMT_E4M3, x, x_sf)
+    if bf16_layer:
+        x = xf.view(T, H).to(torch.bfloat16)
+    else:
+        x = torch.empty(T, H, dtype=torch.uint8, device=dev)
+        x_sf = torch.empty(T, H // 32, dtype=torch.uint8, device=dev)
+        quant(xf, T, H, mm.MM_FMT_E4M3, x, x_sf)
     del xf
     idx_np, w_np, _ = synth.routing(cfg, seed)
     topk_idx = torch.from_numpy(idx_np).to(dev)
     topk_w = torch.from_numpy(w_np).to(dev)
     y = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
-    ws_bytes = mm.mm_workspace_size(T, E, k, H, I)
+    ws_bytes = (mm.mm_bf16_workspace_size if bf16_layer else mm.mm_workspace_size)(T, E, k, H, I)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     torch.cuda.synchronize(dev)
 
     def step():
-        rc = mm.mm_forward(T, E, k, H, I, x, x_sf, topk_idx, topk_w, l1_w, l1_sf, l2_w, l2_sf, y, cfg.clamp, 0,
-                           ws, ws_bytes, stream)
+        if bf16_layer:
+            rc = mm.mm_bf16_forward(T, E, k, H, I, x, topk_idx, topk_w, l1_w, l2_w, y, cfg.clamp, 0, ws, ws_bytes,
+                                    stream)
+        else:
+            rc = mm.mm_forward(T, E, k, H, I, x, x_sf, topk_idx, topk_w, l1_w, l1_sf, l2_w, l2_sf, y, cfg.clamp, 0,
+                               ws, ws_bytes, stream)
         if rc != mm.MM_OK:
             raise RuntimeError(f"mm_forward: {mm.STATUS_NAMES.get(rc, rc)}")
 
@@ -269,7 +289,7 @@ def run_ours(args, rank, world, local_rank):
 
     # ---- end to end through the C ABI: pinned host inputs -> device -> layer -> host
     hx = x.cpu().pin_memory()
-    hsf = x_sf.cpu().pin_memory()
+    hsf = x_sf.cpu().pin_memory() if x_sf is not None else None
     hidx = topk_idx.cpu().pin_memory()
     hw = topk_w.cpu().pin_memory()
     hy = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
@@ -277,7 +297,8 @@ def run_ours(args, rank, world, local_rank):
 
     def e2e_step():
         x.copy_(hx, non_blocking=True)
-        x_sf.copy_(hsf, non_blocking=True)
+        if hsf is not None:
+            x_sf.copy_(hsf, non_blocking=True)
         topk_idx.copy_(hidx, non_blocking=True)
         topk_w.copy_(hw, non_blocking=True)
         step()
@@ -294,21 +315,25 @@ def run_ours(args, rank, world, local_rank):
     e1_.synchronize()
     check_status()
     e2e_tps, e2e_ms = replica_throughput(e0_.elapsed_time(e1_) / e_steps, T, world, max_over_ranks)
-    h2d = hx.numel() + hsf.numel() + hidx.numel() * 4 + hw.numel() * 4
+    h2d = hx.numel() * hx.element_size() + (hsf.numel() if hsf is not None else 0) + hidx.numel() * 4 + hw.numel() * 4
     d2h = hy.numel() * 2
 
     # ---- roofline of the layer kernel (HBM-bound at the decode batch)
     counts = np.bincount(idx_np.reshape(-1)[idx_np.reshape(-1) >= 0], minlength=E)
     touched = int((counts > 0).sum())
-    alg_bytes = (touched * cfg.expert_bytes() + T * H + T * H // 32 + T * k * 8 + T * H * 2)
+    if bf16_layer:      # bf16 weights (no scales), bf16 x
+        alg_bytes = touched * (3 * H * I * 2) + T * H * 2 + T * k * 8 + T * H * 2
+    else:
+        alg_bytes = (touched * cfg.expert_bytes() + T * H + T * H // 32 + T * k * 8 + T * H * 2)
     hbm, bf16, peak_src = _peaks()
     achieved_gbs = alg_bytes / (kernel_ms * 1e-3) / 1e9
     achieved_tflops = cfg.flops() / (kernel_ms * 1e-3) / 1e12
     # E4M3 x E2M1 block-scaled MMAs run at the FP8 rate: the measured bf16 peak x the nominal 2
-    mx_tflops = FP8_PER_BF16 * bf16
+    mx_tflops = bf16 if bf16_layer else FP8_PER_BF16 * bf16
     tensor_bound = cfg.flops() / alg_bytes > (mx_tflops * 1e12) / (hbm * 1e9)
     common = {"peak_source": (f"{peak_src}: MEASURED_PEAKS.json " +
-                              ("bf16_tflops x 2 (nominal FP8 / bf16)" if tensor_bound else "hbm_gbs"))
+                              (("bf16_tflops" if bf16_layer else "bf16_tflops x 2 (nominal FP8 / bf16)")
+                               if tensor_bound else "hbm_gbs"))
               if peak_src == "measured" else "fallback (6.8 TB/s, 1.9 PFLOP/s bf16 x 2)",
               "kernel": "megamoe_kernel", "kernel_ms": round(kernel_ms, 4),
               "algorithmic_bytes_per_launch": alg_bytes, "flops_per_launch": cfg.flops(),
@@ -330,7 +355,7 @@ def run_ours(args, rank, world, local_rank):
 
 
 # ------------------------------------------------------------------ oracle
-def run_oracle_sample(workload, sample_tokens, time_budget_s=25.0):
+def run_oracle_sample(workload, sample_tokens, time_budget_s=25.0, layer="fp8"):
     """Time the CPU oracle (fp64, plain numpy) on the first tokens of the same
     workload.  Returns (tokens/s, threads, sample description)."""
     import numpy as np
@@ -338,18 +363,26 @@ def run_oracle_sample(workload, sample_tokens, time_budget_s=25.0):
     import synth
     from oracle import formats as OF
     from oracle import moe as OM
+    from oracle import moe_bf16 as OMB
 
     cfg = synth.CONFIGS[workload]
     idx, w, _ = synth.routing(cfg)
     n = max(1, sample_tokens)
     toks = list(range(min(n, cfg.T)))
-    xc, xsf = OF.quantize_mx(synth.x_f32(cfg, rows=toks), OF.E4M3)
     experts = sorted({int(e) for e in idx[toks].reshape(-1) if e >= 0})
     tp = time.perf_counter()
-    cache = {e: OM.quantize_expert(synth.w1_f32(cfg, e), synth.w2_f32(cfg, e)) for e in experts}
+    if layer == "bf16":
+        xb = OF.bf16_round(synth.x_f32(cfg, rows=toks))
+        cache = {e: (OF.bf16_round(synth.w1_f32(cfg, e)), OF.bf16_round(synth.w2_f32(cfg, e))) for e in experts}
+    else:
+        xc, xsf = OF.quantize_mx(synth.x_f32(cfg, rows=toks), OF.E4M3)
+        cache = {e: OM.quantize_expert(synth.w1_f32(cfg, e), synth.w2_f32(cfg, e)) for e in experts}
     _log(f"oracle sample: {len(experts)} experts prepared in {time.perf_counter() - tp:.1f} s")
     t0 = time.perf_counter()
-    OM.moe_forward(xc, xsf, idx[toks], w[toks], lambda e: cache[e], cfg.clamp, cfg.E)
+    if layer == "bf16":
+        OMB.moe_forward_bf16(xb, idx[toks], w[toks], lambda e: cache[e], cfg.clamp, cfg.E)
+    else:
+        OM.moe_forward(xc, xsf, idx[toks], w[toks], lambda e: cache[e], cfg.clamp, cfg.E)
     dt = time.perf_counter() - t0
     threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
     desc = (f"first {len(toks)} token(s) of the {workload} batch ({len(experts)} experts, "
@@ -365,6 +398,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode")
+    ap.add_argument("--layer", choices=["fp8", "bf16"], default="fp8",
+                    help="fp8: E4M3 x E2M1 (the default); bf16: the bf16 x bf16 layer")
     ap.add_argument("--cpu-sample-tokens", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tokens", type=int, default=0, help="override the token count (profiling of small cases)")
@@ -387,7 +422,9 @@ def main():
         synth.CONFIGS[cfg.name] = cfg
         args.workload = cfg.name
     config = {"workload": f"{cfg.name}: {cfg.T} tokens, hidden {cfg.H}, inter {cfg.I}, {cfg.E} experts, "
-                          f"top-{cfg.k}, E4M3 x E2M1 with UE8M0/32, clamp {cfg.clamp if cfg.clamp else 'none'}",
+                          f"top-{cfg.k}, "
+                          f"{'bf16 x bf16' if args.layer == 'bf16' else 'E4M3 x E2M1 with UE8M0/32'}, "
+                          f"clamp {cfg.clamp if cfg.clamp else 'none'}",
               "tokens": cfg.T, "hidden": cfg.H, "inter": cfg.I, "experts": cfg.E, "topk": cfg.k,
               "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
               "l2": "inputs larger than L2 (expert weights far exceed 129 MB); no flush"}
@@ -395,7 +432,7 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return 0
-        tps, threads, desc, dt = run_oracle_sample(args.workload, args.cpu_sample_tokens)
+        tps, threads, desc, dt = run_oracle_sample(args.workload, args.cpu_sample_tokens, layer=args.layer)
         line = {"impl": "reference", "metric": METRIC, "value": round(tps, 4), "unit": UNIT, "n_gpus": args.gpus,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * cfg.T / tps, 3),
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -417,7 +454,7 @@ def main():
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         try:
-            tps, threads, desc, dt = run_oracle_sample(args.workload, args.cpu_sample_tokens)
+            tps, threads, desc, dt = run_oracle_sample(args.workload, args.cpu_sample_tokens, layer=args.layer)
             cpu = {"value": round(tps, 4), "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc,
                    "seconds": round(dt, 2)}
         except Exception as exc:  # the baseline must never hide the GPU number
@@ -431,7 +468,8 @@ def main():
         return 0
     line = {"metric": METRIC, "value": round(res["tokens_per_s"], 1), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(res["ms"], 4),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3xe2m1->f32",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16xbf16->f32" if args.layer == "bf16" else "e4m3xe2m1->f32",
             "data": "synthetic", "config": config, "roofline": res["roofline"], "cpu_baseline": cpu,
             "e2e": res["e2e"], "gpu_launches": res["gpu_launches"], "clocks": res["clocks"],
             "route_ms": round(res["route_ms"], 4), "step_ms_percentiles": res["step_ms"]}

@@ -153,6 +153,33 @@ int mm_forward_bf16(int num_tokens, int experts, int topk, int hidden, int inter
                     void* workspace, size_t workspace_bytes, mm_stream_t stream);
 
 /*
+ * mm_bf16_workspace_size / mm_bf16_forward -- the bf16 x bf16 layer: the
+ * second MegaMoE kernel of the pages, the BF16 one whose dispatch, readiness
+ * and combine protocol DeepGEMM PR #451 fixes together with the FP8/FP4 one
+ * (description: "both FP8/FP4 and BF16 kernels"; validation: BF16 graph
+ * replay equal to eager).  The pages give its protocol, not its arithmetic;
+ * the layer computed here is that of mm_forward with every quantisation step
+ * replaced by bfloat16:
+ *
+ *   x      bfloat16   [T, H]       16-byte aligned
+ *   l1_w   bfloat16   [E, 2I, H]   rows [0, I) gate, [I, 2I) up; 32-byte aligned
+ *   l2_w   bfloat16   [E, H, I]    32-byte aligned
+ *   a1 = x . W1[e]^T and o = h . W2[e]^T accumulate in fp32; the clamp and
+ *   SwiGLU are those of mm_forward; the L1 activations h are rounded to
+ *   bfloat16 (nearest even); y = bf16(sum over j ascending of topk_w * o).
+ *
+ * topk_idx, topk_w, y, clamp, num_sms, stream and the error behaviour are
+ * those of mm_forward.  The workspace (mm_bf16_workspace_size bytes, same
+ * alignment and ownership rules) holds activations of 2 bytes per element;
+ * mm_get_status reads its status word as for mm_forward.
+ */
+size_t mm_bf16_workspace_size(int max_tokens, int experts, int topk, int hidden, int inter);
+int mm_bf16_forward(int num_tokens, int experts, int topk, int hidden, int inter,
+                    const void* x, const int32_t* topk_idx, const float* topk_w,
+                    const void* l1_w, const void* l2_w, void* y, float clamp, int num_sms,
+                    void* workspace, size_t workspace_bytes, mm_stream_t stream);
+
+/*
  * mm_set_reserved_sms -- SMs left free for other streams by every launch
  * ([P1] Summary: two by default; [P2] 实现拆解 item 1: 0 disables it).
  * n < 0 is taken as 0.  Process-wide; read at each launch.  Returns the

@@ -51,6 +51,8 @@ _SIGS = {
     "mm_quantize_mx": (_c_int, [_c_vp, _c_ll, _c_ll, _c_int, _c_vp, _c_vp, _c_vp]),
     "mm_forward_noalloc": (_c_int, [_c_int] * 5 + [_c_vp] * 9 + [ctypes.c_float, _c_int, _c_vp]),
     "mm_forward_bf16": (_c_int, [_c_int] * 5 + [_c_vp] * 8 + [ctypes.c_float, _c_int, _c_vp, _c_size, _c_vp]),
+    "mm_bf16_workspace_size": (_c_size, [_c_int] * 5),
+    "mm_bf16_forward": (_c_int, [_c_int] * 5 + [_c_vp] * 6 + [ctypes.c_float, _c_int, _c_vp, _c_size, _c_vp]),
 }
 
 
@@ -115,6 +117,20 @@ def mm_forward_bf16(num_tokens, experts, topk, hidden, inter, x_bf16, topk_idx, 
     return lib().mm_forward_bf16(num_tokens, experts, topk, hidden, inter, _ptr(x_bf16), _ptr(topk_idx),
                                  _ptr(topk_w), _ptr(l1_w), _ptr(l1_sf), _ptr(l2_w), _ptr(l2_sf), _ptr(y),
                                  float(clamp), num_sms, _ptr(workspace), workspace_bytes, _stream(stream))
+
+
+def mm_bf16_workspace_size(max_tokens, experts, topk, hidden, inter) -> int:
+    return lib().mm_bf16_workspace_size(max_tokens, experts, topk, hidden, inter)
+
+
+def mm_bf16_forward(num_tokens, experts, topk, hidden, inter, x, topk_idx, topk_w, l1_w, l2_w, y, clamp,
+                    num_sms, workspace, workspace_bytes=None, stream=None) -> int:
+    """The bf16 x bf16 layer (bf16 activations and weights, no scale factors)."""
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    return lib().mm_bf16_forward(num_tokens, experts, topk, hidden, inter, _ptr(x), _ptr(topk_idx), _ptr(topk_w),
+                                 _ptr(l1_w), _ptr(l2_w), _ptr(y), float(clamp), num_sms, _ptr(workspace),
+                                 workspace_bytes, _stream(stream))
 
 
 def mm_set_reserved_sms(n) -> int:

@@ -65,8 +65,10 @@ struct DevState {
 // Kernel variant for a batch: with at most 16 assignments per expert on
 // average (decode), the thin variant's deeper weight ring; otherwise the wide
 // variant's 128-token tiles.
-int pick_variant(long long assignments, int experts) {
-  return assignments <= 16ll * experts ? kVariantThin : kVariantWide;
+int pick_variant(long long assignments, int experts, bool bf16_layer) {
+  const bool thin = assignments <= 16ll * experts;
+  if (bf16_layer) return thin ? kVariantBf16Thin : kVariantBf16Wide;
+  return thin ? kVariantThin : kVariantWide;
 }
 std::mutex g_mu;
 DevState g_dev[128];
@@ -131,7 +133,7 @@ int encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t
 int launch_route(int T, int E, int k, const int32_t* topk_idx, uint8_t* ws, const Layout& L, cudaStream_t st) {
   RouteParams rp;
   rp.T = T; rp.E = E; rp.k = k; rp.A = T * k;
-  rp.max_n = layer_max_rows(pick_variant((long long)T * k, E));
+  rp.max_n = layer_max_rows(pick_variant((long long)T * k, E, false));   // the same rows for both layers
   rp.topk_idx = topk_idx;
   rp.ws = ws;
   rp.L = L;
@@ -140,11 +142,12 @@ int launch_route(int T, int E, int k, const int32_t* topk_idx, uint8_t* ws, cons
   return MM_OK;
 }
 
-int common_checks(int T, int E, int k, int H, int I, const void* workspace, size_t workspace_bytes, Layout* L) {
+int common_checks(int T, int E, int k, int H, int I, const void* workspace, size_t workspace_bytes, Layout* L,
+                  int esz = 1) {
   int rc = check_shape(T, E, k, H, I);
   if (rc != MM_OK) return rc;
   if (!workspace || !aligned(workspace, 256)) return MM_ERR_INVALID_ARG;
-  *L = make_layout(T, E, k, H, I);
+  *L = make_layout(T, E, k, H, I, esz);
   if (workspace_bytes < L->total) return MM_ERR_WORKSPACE_TOO_SMALL;
   return MM_OK;
 }
@@ -184,10 +187,12 @@ int mm_grid_size(int device_sms, int reserved_sms, int num_sms, int max_resident
 void mm_set_wait_timeout_ns(unsigned long long ns) { g_timeout_ns.store(ns ? ns : kDefaultTimeoutNs); }
 unsigned long long mm_get_wait_timeout_ns(void) { return g_timeout_ns.load(); }
 
-// The fused layer on E4M3 activations (x, x_sf) when x_bf16 is null, else on
-// bf16 activations quantised in the dispatch.  A missing input of either kind
-// is MM_ERR_INVALID_ARG (after the shape checks and the T = 0 early return).
-static int forward_impl(int num_tokens, int experts, int topk, int hidden, int inter,
+// The fused layer.  FP8 x FP4 layer (bf16_layer false): E4M3 activations
+// (x, x_sf) when x_bf16 is null, else bf16 activations quantised in the
+// dispatch.  bf16 x bf16 layer (bf16_layer true): bf16 activations in x and
+// bf16 weights, no scale factors.  A missing input is MM_ERR_INVALID_ARG
+// (after the shape checks and the T = 0 early return).
+static int forward_impl(bool bf16_layer, int num_tokens, int experts, int topk, int hidden, int inter,
                         const void* x, const void* x_sf, const void* x_bf16, const int32_t* topk_idx,
                         const float* topk_w, const void* l1_w, const void* l1_sf, const void* l2_w,
                         const void* l2_sf, void* y, float clamp, int num_sms,
@@ -196,23 +201,26 @@ static int forward_impl(int num_tokens, int experts, int topk, int hidden, int i
   int rc = check_shape(T, E, k, H, I);
   if (rc != MM_OK) return rc;
   if (T == 0) return MM_OK;
-  const bool fp8_in = x_bf16 == nullptr;
-  if ((fp8_in && (!x || !x_sf)) || !topk_idx || !topk_w || !l1_w || !l1_sf || !l2_w || !l2_sf || !y)
+  const bool fp8_in = !bf16_layer && x_bf16 == nullptr;
+  const bool scales = !bf16_layer;
+  if ((bf16_layer && !x) || (fp8_in && (!x || !x_sf)) || !topk_idx || !topk_w || !l1_w || !l2_w || !y ||
+      (scales && (!l1_sf || !l2_sf)))
     return MM_ERR_INVALID_ARG;
-  if ((fp8_in && (!aligned(x, 16) || !aligned(x_sf, 4))) || (!fp8_in && !aligned(x_bf16, 16)) ||
-      !aligned(topk_idx, 4) || !aligned(topk_w, 4) || !aligned(l1_w, 32) || !aligned(l1_sf, 4) ||
-      !aligned(l2_w, 32) || !aligned(l2_sf, 4) || !aligned(y, 16))
+  if ((bf16_layer && !aligned(x, 16)) || (fp8_in && (!aligned(x, 16) || !aligned(x_sf, 4))) ||
+      (!bf16_layer && !fp8_in && !aligned(x_bf16, 16)) || !aligned(topk_idx, 4) || !aligned(topk_w, 4) ||
+      !aligned(l1_w, 32) || !aligned(l2_w, 32) || (scales && (!aligned(l1_sf, 4) || !aligned(l2_sf, 4))) ||
+      !aligned(y, 16))
     return MM_ERR_INVALID_ARG;
   if (std::isnan(clamp)) return MM_ERR_INVALID_ARG;
   Layout L;
-  rc = common_checks(T, E, k, H, I, workspace, workspace_bytes, &L);
+  rc = common_checks(T, E, k, H, I, workspace, workspace_bytes, &L, bf16_layer ? 2 : 1);
   if (rc != MM_OK) return rc;
 
   int dev;
   DevState* st;
   rc = device_state(&dev, &st);
   if (rc != MM_OK) return rc;
-  const int variant = pick_variant((long long)T * k, E);
+  const int variant = pick_variant((long long)T * k, E, bf16_layer);
   const int grid = mm_grid_size(st->sms, reserved_now(), num_sms, st->max_resident[variant]);
   const int A = T * k;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -221,7 +229,18 @@ static int forward_impl(int num_tokens, int experts, int topk, int hidden, int i
   // in shared memory); dispatched tokens and L1 activations as [A][K] bytes,
   // 16-row and 128-row boxes.
   alignas(64) CUtensorMap maps[6];
-  if (encode_2d(&maps[0], CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, l1_w, (uint64_t)H, (uint64_t)E * 2 * I, H / 2,
+  // bf16 layer: every operand bf16, [rows][K] with 64-element (128-byte) boxes
+  const int kk = bf16_layer ? kBlockK / 2 : kBlockK;
+  if (bf16_layer) {
+    const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    if (encode_2d(&maps[0], bf, l1_w, (uint64_t)H, (uint64_t)E * 2 * I, (uint64_t)H * 2, kk, 128) != MM_OK ||
+        encode_2d(&maps[1], bf, l2_w, (uint64_t)I, (uint64_t)E * H, (uint64_t)I * 2, kk, 128) != MM_OK ||
+        encode_2d(&maps[2], bf, ws + L.xs, (uint64_t)H, (uint64_t)A, (uint64_t)H * 2, kk, 16) != MM_OK ||
+        encode_2d(&maps[3], bf, ws + L.xs, (uint64_t)H, (uint64_t)A, (uint64_t)H * 2, kk, kTileM) != MM_OK ||
+        encode_2d(&maps[4], bf, ws + L.l1a, (uint64_t)I, (uint64_t)A, (uint64_t)I * 2, kk, 16) != MM_OK ||
+        encode_2d(&maps[5], bf, ws + L.l1a, (uint64_t)I, (uint64_t)A, (uint64_t)I * 2, kk, kTileM) != MM_OK)
+      return MM_ERR_CUDA;
+  } else if (encode_2d(&maps[0], CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, l1_w, (uint64_t)H, (uint64_t)E * 2 * I, H / 2,
                 kBlockK, 128) != MM_OK ||
       encode_2d(&maps[1], CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, l2_w, (uint64_t)I, (uint64_t)E * H, I / 2,
                 kBlockK, 128) != MM_OK ||
@@ -240,14 +259,14 @@ static int forward_impl(int num_tokens, int experts, int topk, int hidden, int i
   ForwardParams fp;
   fp.T = T; fp.E = E; fp.k = k; fp.H = H; fp.I = I; fp.A = A;
   fp.mt1 = I / kL1Feat; fp.mt2 = (H + kTileN - 1) / kTileN;
-  fp.ks1 = H / kBlockK; fp.ks2 = I / kBlockK;
+  fp.ks1 = H / kk; fp.ks2 = I / kk;
   fp.use_clamp = (std::isfinite(clamp) && clamp > 0.f) ? 1 : 0;
   fp.clamp = fp.use_clamp ? clamp : 0.f;
   fp.a_box128 = A >= kTileM ? 1 : 0;
   fp.timeout_ns = g_timeout_ns.load();
-  fp.x = fp8_in ? static_cast<const uint8_t*>(x) : nullptr;
+  fp.x = (fp8_in || bf16_layer) ? static_cast<const uint8_t*>(x) : nullptr;
   fp.x_sf = fp8_in ? static_cast<const uint8_t*>(x_sf) : nullptr;
-  fp.x_bf16 = fp8_in ? nullptr : static_cast<const uint16_t*>(x_bf16);
+  fp.x_bf16 = (fp8_in || bf16_layer) ? nullptr : static_cast<const uint16_t*>(x_bf16);
   fp.topk_idx = topk_idx;
   fp.topk_w = topk_w;
   fp.w1_sf = static_cast<const uint8_t*>(l1_sf);
@@ -264,8 +283,8 @@ int mm_forward(int num_tokens, int experts, int topk, int hidden, int inter,
                const void* l1_w, const void* l1_sf, const void* l2_w, const void* l2_sf,
                void* y, float clamp, int num_sms,
                void* workspace, size_t workspace_bytes, mm_stream_t stream) {
-  return forward_impl(num_tokens, experts, topk, hidden, inter, x, x_sf, nullptr, topk_idx, topk_w, l1_w, l1_sf,
-                      l2_w, l2_sf, y, clamp, num_sms, workspace, workspace_bytes, stream);
+  return forward_impl(false, num_tokens, experts, topk, hidden, inter, x, x_sf, nullptr, topk_idx, topk_w, l1_w,
+                      l1_sf, l2_w, l2_sf, y, clamp, num_sms, workspace, workspace_bytes, stream);
 }
 
 int mm_forward_bf16(int num_tokens, int experts, int topk, int hidden, int inter,
@@ -273,8 +292,21 @@ int mm_forward_bf16(int num_tokens, int experts, int topk, int hidden, int inter
                     const void* l1_w, const void* l1_sf, const void* l2_w, const void* l2_sf,
                     void* y, float clamp, int num_sms,
                     void* workspace, size_t workspace_bytes, mm_stream_t stream) {
-  return forward_impl(num_tokens, experts, topk, hidden, inter, nullptr, nullptr, x_bf16, topk_idx, topk_w, l1_w,
-                      l1_sf, l2_w, l2_sf, y, clamp, num_sms, workspace, workspace_bytes, stream);
+  return forward_impl(false, num_tokens, experts, topk, hidden, inter, nullptr, nullptr, x_bf16, topk_idx, topk_w,
+                      l1_w, l1_sf, l2_w, l2_sf, y, clamp, num_sms, workspace, workspace_bytes, stream);
+}
+
+size_t mm_bf16_workspace_size(int max_tokens, int experts, int topk, int hidden, int inter) {
+  if (check_shape(max_tokens, experts, topk, hidden, inter) != MM_OK) return 0;
+  return make_layout(max_tokens, experts, topk, hidden, inter, 2).total;
+}
+
+int mm_bf16_forward(int num_tokens, int experts, int topk, int hidden, int inter,
+                    const void* x, const int32_t* topk_idx, const float* topk_w,
+                    const void* l1_w, const void* l2_w, void* y, float clamp, int num_sms,
+                    void* workspace, size_t workspace_bytes, mm_stream_t stream) {
+  return forward_impl(true, num_tokens, experts, topk, hidden, inter, x, nullptr, nullptr, topk_idx, topk_w, l1_w,
+                      nullptr, l2_w, nullptr, y, clamp, num_sms, workspace, workspace_bytes, stream);
 }
 
 int mm_route(int num_tokens, int experts, int topk, int hidden, int inter, const int32_t* topk_idx,

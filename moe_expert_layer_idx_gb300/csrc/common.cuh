@@ -51,11 +51,19 @@ constexpr uint32_t kSFSetCols = 12;                 // SFA: +0..3, SFB: +4..11
 // epilogue thread reads.  Its ring is half again as deep, which is what a
 // decode batch (a few tokens per expert, weight streaming) needs.  The wide
 // variant adds the epilogue's transpose buffers (see kXposeBytes).
-template <int kARows_, int kStages_, bool kXpose_>
+//
+// kBf16 selects the bf16 x bf16 layer: bf16 activations and weights, no scale
+// factors, tcgen05.mma kind::f16, bf16 L1 activations.  Its K stage is 64
+// elements, so rows stay 128 bytes and every shared-memory footprint and box
+// byte count of a stage is that of the FP8 x FP4 layer.
+template <int kARows_, int kStages_, bool kXpose_, bool kBf16_>
 struct Variant {
   static constexpr int kARows = kARows_;
   static constexpr int kStages = kStages_;
   static constexpr bool kXpose = kXpose_;
+  static constexpr bool kBf16 = kBf16_;
+  static constexpr int kKStage = kBf16 ? kBlockK / 2 : kBlockK;     // K elements per stage
+  static constexpr int kWeightBoxTx = kBf16 ? 128 * 128 : kBHalfTxBytes;   // one 128-row weight box
   static constexpr int kABytes = kARows * kBlockK;
   static constexpr int kStageBytes = kABytes + kBBytes + kSFABytes + kSFBBytes;
   // Epilogue transpose buffer per warp: 32 token rows x 16 fp32 columns, so the
@@ -73,9 +81,13 @@ struct Variant {
   // the MMA's 128-row A window of the last stage stays inside the allocation
   static_assert((kStages - 1) * kABytes + kTileM * kBlockK <= kStages * kStageBytes, "A window");
 };
-using WideVariant = Variant<128, 4, true>;
-using ThinVariant = Variant<32, 6, false>;
-enum VariantId : int { kVariantWide = 0, kVariantThin = 1, kNumVariants = 2 };
+using WideVariant = Variant<128, 4, true, false>;
+using ThinVariant = Variant<32, 6, false, false>;
+using Bf16WideVariant = Variant<128, 4, true, true>;
+using Bf16ThinVariant = Variant<32, 6, false, true>;
+enum VariantId : int {
+  kVariantWide = 0, kVariantThin = 1, kVariantBf16Wide = 2, kVariantBf16Thin = 3, kNumVariants = 4
+};
 
 
 // ----------------------------------------------------------------- control block
@@ -99,7 +111,9 @@ struct Layout {
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-__host__ __device__ inline Layout make_layout(long long T, int E, int k, int H, int I) {
+// esz: bytes per activation element (1: E4M3 codes with UE8M0 scales; 2: bf16,
+// whose scale regions stay unused).
+__host__ __device__ inline Layout make_layout(long long T, int E, int k, int H, int I, int esz = 1) {
   Layout L;
   const size_t A = (size_t)T * (size_t)k;
   size_t o = 0;
@@ -111,9 +125,9 @@ __host__ __device__ inline Layout make_layout(long long T, int E, int k, int H, 
   L.l1_done = o;  o = align256(o + 4 * (size_t)E);
   L.perm = o;     o = align256(o + 4 * A);
   L.inv = o;      o = align256(o + 4 * A);
-  L.xs = o;       o = align256(o + A * (size_t)H);
+  L.xs = o;       o = align256(o + A * (size_t)H * esz);
   L.xs_sf = o;    o = align256(o + A * (size_t)(H / 32));
-  L.l1a = o;      o = align256(o + A * (size_t)I);
+  L.l1a = o;      o = align256(o + A * (size_t)I * esz);
   L.l1a_sf = o;   o = align256(o + A * (size_t)(I / 32));
   L.stage = o;    o = align256(o + A * (size_t)H * 4);
   L.total = o;
@@ -387,6 +401,28 @@ __device__ __forceinline__ uint32_t idesc_mx(uint32_t n, uint32_t sf_id) {
   d |= (128u >> 4) << 24;          // M / 16
   d |= sf_id << 29;                // A scale-factor id
   return d;
+}
+
+// Instruction descriptor of kind::f16: A = bf16 tokens (M = 128), B = bf16
+// weights (N), fp32 accumulator, both K-major.
+__device__ __forceinline__ uint32_t idesc_bf16(uint32_t n) {
+  uint32_t d = 0;
+  d |= 1u << 4;                    // accumulator format: F32
+  d |= 1u << 7;                    // A format: BF16
+  d |= 1u << 10;                   // B format: BF16
+  d |= (n >> 3) << 17;             // N / 8
+  d |= (128u >> 4) << 24;          // M / 16
+  return d;
+}
+// D (+)= A . B^T, bf16 operands (K = 16 per instruction).
+__device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+      :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
 }
 
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {

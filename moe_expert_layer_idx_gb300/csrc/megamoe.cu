@@ -210,7 +210,7 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 2 + 1);
+      mbar_init(&full[s], V::kBf16 ? 2 : 2 + 1);      // producers (+ the scale loader)
       mbar_init(&empty[s], 1);
     }
     mbar_init(tfull, 1);
@@ -239,8 +239,8 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
   const uint32_t tmem = s_misc[0];
 
   // ------------------------------------------------------------ 0. dispatch
-  if (p.x_bf16 != nullptr) {
-    // bf16 activations: one warp per token reads its row once; lane b quantises
+  if (!V::kBf16 && p.x_bf16 != nullptr) {
+    // bf16 activations of the FP8 x FP4 layer: one warp per token reads its row once; lane b quantises
     // 32-element blocks b, b + 32, ... (E4M3 + UE8M0 by the scale rule of the
     // L1 epilogue) and writes each block to every slot of the token, then each
     // slot's expert arrival count is released.
@@ -296,13 +296,14 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
   } else {
     const int nvalid = __ldg(offsets + p.E);
     const int H = p.H;
-    const int nvec = H / 16, nsf = H / 128;
+    constexpr int esz = V::kBf16 ? 2 : 1;          // bytes per activation element
+    const int nvec = H * esz / 16, nsf = H / 128;
     for (int s = blockIdx.x * (kThreads / 32) + warp; s < nvalid; s += gridDim.x * (kThreads / 32)) {
       const int f = __ldg(perm + s);
       const int t = f / p.k;
       const int e = __ldg(p.topk_idx + f);
-      const uint4* src = reinterpret_cast<const uint4*>(p.x + (size_t)t * H);
-      uint4* dst = reinterpret_cast<uint4*>(xs + (size_t)s * H);
+      const uint4* src = reinterpret_cast<const uint4*>(p.x + (size_t)t * H * esz);
+      uint4* dst = reinterpret_cast<uint4*>(xs + (size_t)s * H * esz);
       for (int c0 = lane; c0 < nvec; c0 += 32 * 8) {       // 8 independent loads in flight per lane
         uint4 v[8];
 #pragma unroll
@@ -312,9 +313,11 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
         for (int i = 0; i < 8; ++i)
           if (c0 + 32 * i < nvec) dst[c0 + 32 * i] = v[i];
       }
-      const uint32_t* ssf = reinterpret_cast<const uint32_t*>(p.x_sf + (size_t)t * (H / 32));
-      uint32_t* dsf = reinterpret_cast<uint32_t*>(xs_sf + (size_t)s * (H / 32));
-      for (int c = lane; c < nsf; c += 32) dsf[c] = __ldg(ssf + c);
+      if (!V::kBf16) {
+        const uint32_t* ssf = reinterpret_cast<const uint32_t*>(p.x_sf + (size_t)t * (H / 32));
+        uint32_t* dsf = reinterpret_cast<uint32_t*>(xs_sf + (size_t)s * (H / 32));
+        for (int c = lane; c < nsf; c += 32) dsf[c] = __ldg(ssf + c);
+      }
       fence_proxy_async_global();
       __threadfence();
       __syncwarp();
@@ -360,7 +363,7 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
         const int nbox = ti.m16 / 16;
         const int my_a_bytes = full_box ? (pid == 0 ? kABytes : 0) : ((nbox + 1 - pid) / 2) * 16 * kBlockK;
         const bool my_b = pid == 0 || ti.n > 128;
-        const uint32_t bytes = (uint32_t)((my_b ? kBHalfTxBytes : 0) + my_a_bytes);
+        const uint32_t bytes = (uint32_t)((my_b ? V::kWeightBoxTx : 0) + my_a_bytes);
         const CUtensorMap* tm_b = ti.layer == 1 ? &tm_w1 : &tm_w2;
         const CUtensorMap* tm_a = ti.layer == 1 ? (full_box ? &tm_xs128 : &tm_xs16)
                                                 : (full_box ? &tm_l1a128 : &tm_l1a16);
@@ -372,7 +375,7 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
           mbar_arrive_expect_tx(fb, bytes);
           const uint32_t a_dst = smem_u32(sA + stage * kABytes);
           const uint32_t b_dst = smem_u32(sB + stage * kBBytes) + (uint32_t)(pid * 128 * kBlockK);
-          const int kx = kb * kBlockK;
+          const int kx = kb * V::kKStage;
           if (my_b) tma_load_2d(b_dst, tm_b, fb, kx, b_row);
           if (full_box) {
             if (pid == 0) tma_load_2d(a_dst, tm_a, fb, kx, ti.r0);
@@ -409,20 +412,28 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
         const uint32_t id2 = id0 | (2u << 4) | (2u << 29);
         const uint32_t id3 = id0 | (3u << 4) | (3u << 29);
         const bool two_sfb = ti.n > 128;
+        const uint32_t idb = idesc_bf16((uint32_t)ti.n);
         for (int kb = 0; kb < ti.ks; ++kb) {
           if (!mbar_wait(full0 + stage * 8u, phase, ctrl, to, (kSiteFull << 24) | tag)) { ok = false; break; }
           const uint32_t so = stage;
-          const uint64_t sfb_d = sfb_desc0 + (uint64_t)(so * (uint32_t)(kSFBBytes >> 4));
-          const uint32_t sfa_t = tmem + kSFCol0 + so * kSFSetCols, sfb_t = sfa_t + 4;
-          tc_cp_sf(sfa_t, sfa_desc0 + (uint64_t)(so * (uint32_t)(kSFABytes >> 4)));
-          tc_cp_sf(sfb_t, sfb_d);
-          if (two_sfb) tc_cp_sf(sfb_t + 4, sfb_d + (512 >> 4));
           const uint64_t ad = a_desc0 + (uint64_t)(so * (uint32_t)(kABytes >> 4));
           const uint64_t bd = b_desc0 + (uint64_t)(so * (uint32_t)(kBBytes >> 4));
-          tc_mma_mx(tmem, ad, bd, id0, sfa_t, sfb_t, kb != 0 ? 1u : 0u);
-          tc_mma_mx_acc(tmem, ad + 2, bd + 2, id1, sfa_t, sfb_t);     // +32 bytes along K
-          tc_mma_mx_acc(tmem, ad + 4, bd + 4, id2, sfa_t, sfb_t);
-          tc_mma_mx_acc(tmem, ad + 6, bd + 6, id3, sfa_t, sfb_t);
+          if constexpr (V::kBf16) {
+            tc_mma_f16(tmem, ad, bd, idb, kb != 0 ? 1u : 0u);            // K = 16 each: +32 bytes
+            tc_mma_f16(tmem, ad + 2, bd + 2, idb, 1u);
+            tc_mma_f16(tmem, ad + 4, bd + 4, idb, 1u);
+            tc_mma_f16(tmem, ad + 6, bd + 6, idb, 1u);
+          } else {
+            const uint64_t sfb_d = sfb_desc0 + (uint64_t)(so * (uint32_t)(kSFBBytes >> 4));
+            const uint32_t sfa_t = tmem + kSFCol0 + so * kSFSetCols, sfb_t = sfa_t + 4;
+            tc_cp_sf(sfa_t, sfa_desc0 + (uint64_t)(so * (uint32_t)(kSFABytes >> 4)));
+            tc_cp_sf(sfb_t, sfb_d);
+            if (two_sfb) tc_cp_sf(sfb_t + 4, sfb_d + (512 >> 4));
+            tc_mma_mx(tmem, ad, bd, id0, sfa_t, sfb_t, kb != 0 ? 1u : 0u);
+            tc_mma_mx_acc(tmem, ad + 2, bd + 2, id1, sfa_t, sfb_t);     // K = 32 each: +32 bytes
+            tc_mma_mx_acc(tmem, ad + 4, bd + 4, id2, sfa_t, sfb_t);
+            tc_mma_mx_acc(tmem, ad + 6, bd + 6, id3, sfa_t, sfb_t);
+          }
           tc_commit(empty0 + stage * 8u);
           ++consumed;
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
@@ -435,6 +446,12 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
       tc_commit(smem_u32(drain));
       if (!mbar_wait_drain(smem_u32(drain), 0, to)) set_error(ctrl, MM_ERR_TIMEOUT, kSiteDrain << 24);
     }
+  } else if (warp == 2 && V::kBf16) {
+    // ---------------- no scale factors in the bf16 layer: only follow the tile feed
+    TileFeed feed(s_tiles, tile_full, tile_empty);
+    bool fed = true;
+    Tile ti;
+    while (feed.take_warp(lane, ctrl, to, fed, ti)) {}
   } else if (warp == 2) {
     // ---------------- scale loader (32 lanes)
     // Each stage's UE8M0 bytes are gathered with cp.async (one commit group per
@@ -576,7 +593,32 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(tempty));
       if (live_warp) {
-        if (ti.layer == 1) {
+        if (V::kBf16 && ti.layer == 1) {
+          // ---- L1 of the bf16 layer: features [64hh, 64hh + 64): clamp + SwiGLU, rounded to bf16
+          const float L = p.clamp;
+          // bf16 pair i/2 goes in place into v[i/2], a gate value already consumed
+#pragma unroll
+          for (int i = 0; i < 64; i += 2) {
+            float hv[2];
+#pragma unroll
+            for (int d = 0; d < 2; ++d) {
+              float gg = v[i + d], uu = v[64 + i + d];
+              if (p.use_clamp) {
+                gg = fminf(gg, L);
+                uu = fminf(fmaxf(uu, -L), L);
+              }
+              hv[d] = gg * __fdividef(1.0f, 1.0f + __expf(-gg)) * uu;   // fast-math SiLU
+            }
+            v[i / 2] = __uint_as_float((uint32_t)bf16_bits_rn(hv[0]) | ((uint32_t)bf16_bits_rn(hv[1]) << 16));
+          }
+          if (valid) {
+            uint4* d4 = reinterpret_cast<uint4*>(l1a + (slot * p.I + ti.nb * kL1Feat + hh * 64) * 2);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              d4[i] = make_uint4(__float_as_uint(v[4 * i]), __float_as_uint(v[4 * i + 1]), __float_as_uint(v[4 * i + 2]),
+                                 __float_as_uint(v[4 * i + 3]));
+          }
+        } else if (ti.layer == 1) {
           // ---- L1: features [64hh, 64hh + 64) of the row: clamp + SwiGLU, then E4M3 + UE8M0 per 32
           const float L = p.clamp;
           uint8_t* dst = l1a + slot * p.I + ti.nb * kL1Feat + hh * 64;
@@ -690,7 +732,7 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
     const uint32_t issued = issued0 > issued1 ? issued0 : issued1;
     for (uint32_t s = consumed; s < issued; ++s) {
       const uint32_t bar = smem_u32(&full[s % kStages]);
-      if (s >= armed) mbar_arrive(bar);
+      if (!V::kBf16 && s >= armed) mbar_arrive(bar);
       if (s >= issued0) mbar_arrive(bar);
       if (s >= issued1) mbar_arrive(bar);
       if (!mbar_wait_drain(bar, (s / kStages) & 1u, to)) set_error(ctrl, MM_ERR_TIMEOUT, kSiteDrain << 24);
@@ -762,26 +804,40 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
 // ---------------------------------------------------------------- host side
 // Template kernels are configured and launched in the translation unit that
 // defines them.
-int layer_max_rows(int variant) { return variant == kVariantThin ? ThinVariant::kARows : WideVariant::kARows; }
+int layer_max_rows(int variant) {
+  return (variant == kVariantThin || variant == kVariantBf16Thin) ? ThinVariant::kARows : WideVariant::kARows;
+}
+
+template <class V>
+static cudaError_t prepare_one(int* ctas_per_sm) {
+  cudaError_t e = cudaFuncSetAttribute(megamoe_kernel<V>, cudaFuncAttributeMaxDynamicSharedMemorySize, V::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, megamoe_kernel<V>, kThreads, V::kSmemBytes);
+}
 
 cudaError_t layer_prepare(int variant, int* ctas_per_sm) {
-  const void* fn = variant == kVariantThin ? (const void*)megamoe_kernel<ThinVariant>
-                                           : (const void*)megamoe_kernel<WideVariant>;
-  const int smem = variant == kVariantThin ? ThinVariant::kSmemBytes : WideVariant::kSmemBytes;
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, fn, kThreads, smem);
+  switch (variant) {
+    case kVariantThin: return prepare_one<ThinVariant>(ctas_per_sm);
+    case kVariantBf16Wide: return prepare_one<Bf16WideVariant>(ctas_per_sm);
+    case kVariantBf16Thin: return prepare_one<Bf16ThinVariant>(ctas_per_sm);
+    default: return prepare_one<WideVariant>(ctas_per_sm);
+  }
+}
+
+template <class V>
+static cudaError_t launch_one(int grid, cudaStream_t stream, const CUtensorMap* maps, const ForwardParams& p) {
+  megamoe_kernel<V><<<grid, kThreads, V::kSmemBytes, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p);
+  return cudaGetLastError();
 }
 
 // maps: W1, W2, dispatched tokens (16- and 128-row boxes), L1 activations (16- and 128-row boxes)
 cudaError_t layer_launch(int variant, int grid, cudaStream_t stream, const CUtensorMap* maps, const ForwardParams& p) {
-  if (variant == kVariantThin)
-    megamoe_kernel<ThinVariant><<<grid, kThreads, ThinVariant::kSmemBytes, stream>>>(maps[0], maps[1], maps[2],
-                                                                                     maps[3], maps[4], maps[5], p);
-  else
-    megamoe_kernel<WideVariant><<<grid, kThreads, WideVariant::kSmemBytes, stream>>>(maps[0], maps[1], maps[2],
-                                                                                     maps[3], maps[4], maps[5], p);
-  return cudaGetLastError();
+  switch (variant) {
+    case kVariantThin: return launch_one<ThinVariant>(grid, stream, maps, p);
+    case kVariantBf16Wide: return launch_one<Bf16WideVariant>(grid, stream, maps, p);
+    case kVariantBf16Thin: return launch_one<Bf16ThinVariant>(grid, stream, maps, p);
+    default: return launch_one<WideVariant>(grid, stream, maps, p);
+  }
 }
 
 }  // namespace mm

@@ -171,6 +171,26 @@ def test_forward_bf16_argument_errors(lib):
     assert _fwd_bf16(workspace_bytes=need - 1) == mm.MM_ERR_WORKSPACE_TOO_SMALL
 
 
+def _bf16_layer(**kw):
+    a = dict(num_tokens=64, experts=8, topk=2, hidden=256, inter=128, x=FAKE, topk_idx=FAKE, topk_w=FAKE,
+             l1_w=FAKE, l2_w=FAKE, y=FAKE, clamp=7.0, num_sms=0, workspace=FAKE, workspace_bytes=1 << 40, stream=0)
+    a.update(kw)
+    return mm.mm_bf16_forward(**a)
+
+
+def test_bf16_layer_workspace_and_argument_errors(lib):
+    fp8 = mm.mm_workspace_size(64, 8, 2, 256, 128)
+    bf = mm.mm_bf16_workspace_size(64, 8, 2, 256, 128)
+    assert bf > fp8                                            # 2-byte activations
+    assert mm.mm_bf16_workspace_size(64, 8, 2, 200, 128) == 0
+    assert _bf16_layer(num_tokens=0) == mm.MM_OK
+    assert _bf16_layer(hidden=200) == mm.MM_ERR_UNSUPPORTED_SHAPE
+    assert _bf16_layer(x=0) == mm.MM_ERR_INVALID_ARG
+    assert _bf16_layer(l2_w=0) == mm.MM_ERR_INVALID_ARG
+    assert _bf16_layer(x=FAKE + 8) == mm.MM_ERR_INVALID_ARG
+    assert _bf16_layer(workspace_bytes=fp8) == mm.MM_ERR_WORKSPACE_TOO_SMALL   # the FP8 layer's size is short
+
+
 def test_route_and_quantize_argument_errors(lib):
     assert mm.mm_route(64, 8, 2, 256, 128, FAKE, FAKE, 10, 0) == mm.MM_ERR_WORKSPACE_TOO_SMALL
     assert mm.mm_route(64, 8, 2, 256, 128, 0, FAKE, 1 << 40, 0) == mm.MM_ERR_INVALID_ARG
@@ -185,3 +205,4 @@ def test_forward_without_device(lib):
         pytest.skip("a GPU is present")
     assert _fwd() == mm.MM_ERR_NO_DEVICE
     assert _fwd_bf16() == mm.MM_ERR_NO_DEVICE
+    assert _bf16_layer() == mm.MM_ERR_NO_DEVICE
