@@ -107,3 +107,46 @@ def test_bf16_layer_empty_rows_are_zero(case):
     empty = np.all(idx < 0, axis=1)
     if empty.any():
         assert torch.all(y[torch.from_numpy(empty).cuda()] == 0)
+
+
+def test_bf16_layer_graph_replays_equal_eager():
+    """The BF16 kernel's graph-replay check of DeepGEMM PR #451 (validation:
+    12 changed-input replays per case equal to eager): capture mm_bf16_forward
+    once, write new tokens and routing (seeds 1..12) into the captured
+    buffers, replay, and compare bit for bit with an eager launch."""
+    cfg = synth.Config("graph-bf16", T=200, H=512, I=256, E=96, k=8, clamp=0.0, skew=True, seed=21)
+    T, H, I, E, k = cfg.T, cfg.H, cfg.I, cfg.E, cfg.k
+    w1 = _device_bf16(cfg.seed, synth.TENSOR_W1, E * 2 * I * H, synth.weight_scale(H)).view(E, 2 * I, H)
+    w2 = _device_bf16(cfg.seed, synth.TENSOR_W2, E * H * I, synth.weight_scale(I)).view(E, H, I)
+
+    def tokens(seed):
+        idx, w, _ = synth.routing(cfg, seed)
+        x = _device_bf16(seed, synth.TENSOR_X, T * H, 1.0).view(T, H)
+        return (x, torch.from_numpy(np.ascontiguousarray(idx, dtype=np.int32)).cuda(),
+                torch.from_numpy(np.ascontiguousarray(w, dtype=np.float32)).cuda())
+
+    x, idx_t, w_t = tokens(0)
+    nbytes = mm.mm_bf16_workspace_size(T, E, k, H, I)
+    ws_g = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    ws_e = torch.empty_like(ws_g)
+    y_g = torch.empty(T, H, dtype=torch.bfloat16, device="cuda")
+    y_e = torch.empty_like(y_g)
+
+    def fwd(y, ws, stream=None):
+        return mm.mm_bf16_forward(T, E, k, H, I, x, idx_t, w_t, w1, w2, y, cfg.clamp, 0, ws, stream=stream)
+
+    assert fwd(y_g, ws_g) == mm.MM_OK
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        assert fwd(y_g, ws_g, torch.cuda.current_stream()) == mm.MM_OK
+    torch.cuda.synchronize()
+    for r in range(1, 13):
+        nx, ni, nw = tokens(r)
+        x.copy_(nx); idx_t.copy_(ni); w_t.copy_(nw)
+        y_g.fill_(float("nan"))
+        graph.replay()
+        assert fwd(y_e, ws_e) == mm.MM_OK
+        torch.cuda.synchronize()
+        assert mm.mm_get_status(ws_g)[0] == mm.MM_OK and mm.mm_get_status(ws_e)[0] == mm.MM_OK
+        assert torch.equal(y_g.view(torch.int16), y_e.view(torch.int16)), f"replay {r}"
