@@ -454,24 +454,15 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
     while (feed.take_warp(lane, ctrl, to, fed, ti)) {}
   } else if (warp == 2) {
     // ---------------- scale loader (32 lanes)
-    // Each stage's UE8M0 bytes are gathered with cp.async (one commit group per
-    // stage).  The tensor core reads the atoms through the async proxy, so a
-    // stage is released only after its copies have landed and every lane has
-    // fenced them: lane 0 then arrives on the stage's full barrier.  The
-    // release trails the issue by kSfLag stages (<= the ring depth, so the
-    // ring always drains), which keeps the copies' latency off the loop; the
-    // held-back stages are released before any wait on another tile's progress.
-    constexpr uint32_t kSfLag = 2;
-    static_assert(kSfLag <= (uint32_t)kStages, "release lag");
-    uint32_t stage = 0, phase = 0, armed = 0, gathered = 0, astage = 0;
-    auto release_oldest = [&](bool all) {
-      if (all) cp_async_wait<0>(); else cp_async_wait<kSfLag - 1>();
-      fence_proxy_async_shared();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&full[astage]));
-      ++armed;
-      if (++astage == (uint32_t)kStages) astage = 0;
-    };
+    // Lane l owns rows l + 32j of the tile's token block (j < 4) and of its
+    // weight rows (two 128-row atoms).  For every group of 4 K stages it loads
+    // each owned row's 4 x 4 scale bytes (16 contiguous bytes: one vector load
+    // where rows are 16-byte aligned) into registers, ahead of the stages.
+    // Then, stage by stage, it writes the stage's bytes into the 32x4x4 atom
+    // layout (one 16-byte shared store per atom and lane), every lane fences
+    // them (the tensor core reads through the async proxy) and lane 0 arrives
+    // on the stage's full barrier.
+    uint32_t stage = 0, phase = 0, armed = 0;
     int ready_key = -1;
     const int H32 = p.H / 32, I32 = p.I / 32;
     TileFeed feed(s_tiles, tile_full, tile_empty);
@@ -483,8 +474,6 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
       bool ok = true;
       const int key = ti.e * 2 + ti.layer - 1;
       if (key != ready_key) {
-        // The dependency may wait on tiles whose MMAs need the stages still held back: release them first.
-        while (armed < gathered) release_oldest(true);
         if (lane == 0) {
           ok = (ti.layer == 1)
                    ? counter_wait(&arrival[ti.e], (uint32_t)__ldg(counts + ti.e), ctrl, to, (kSiteArrival << 24) | tag)
@@ -497,44 +486,74 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
         if (ti.layer == 1) (void)ld_acquire(&arrival[ti.e]); else (void)ld_acquire(&l1_done[ti.e]);
         ready_key = key;
       }
-      // A: the block's token rows; B: the tile's weight rows in two 128-row atoms
       const uint8_t* a_sf_base = ti.layer == 1 ? xs_sf : l1a_sf;
       const uint8_t* b_sf_base = ti.layer == 1 ? p.w1_sf : p.w2_sf;
       const int kstride = ti.layer == 1 ? H32 : I32;
       const int b_row0 = ti.layer == 1 ? ti.e * 2 * p.I + ti.nb * kL1Feat : ti.e * p.H + ti.nb * kTileN;
       const int b_row1 = ti.layer == 1 ? b_row0 + p.I : b_row0 + 128;
       const bool two_sfb = ti.n > 128;
-      for (int kb = 0; kb < ti.ks; ++kb) {
-        bool w = true;
-        if (lane == 0) w = mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, ctrl, to, (kSiteEmpty << 24) | tag);
-        w = __shfl_sync(0xffffffffu, w, 0);
-        if (!w) { ok = false; break; }
-        const uint32_t dA = smem_u32(sSFA + stage * kSFABytes) + lane * 16;
-        const uint32_t dB = smem_u32(sSFB + stage * kSFBBytes) + lane * 16;
+      const bool a_vec = (kstride & 15) == 0;                                    // workspace rows
+      const bool b_vec = a_vec && (reinterpret_cast<uintptr_t>(b_sf_base) & 15) == 0;
+      const uint8_t* a_row[4];
+      const uint8_t* b_row[8];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int slot = min(ti.r0 + lane + 32 * j, p.A - 1);
+        a_row[j] = a_sf_base + (size_t)slot * kstride;
+        b_row[j] = b_sf_base + (size_t)(b_row0 + lane + 32 * j) * kstride;
+        b_row[4 + j] = b_sf_base + (size_t)((two_sfb ? b_row1 : b_row0) + lane + 32 * j) * kstride;
+      }
+      for (int g0 = 0; g0 < ti.ks && ok; g0 += 4) {
+        const int ng = min(4, ti.ks - g0);
+        uint32_t a[4][4], b[8][4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const int m = lane + 32 * j;
-          if (m < ti.m16) {
-            const int slot = min(ti.r0 + m, p.A - 1);
-            cp_async_4(dA + j * 4, a_sf_base + (size_t)slot * kstride + kb * 4);
+          if (lane + 32 * j < ti.m16) {
+            if (a_vec && ng == 4) {
+              const uint4 v = __ldcg(reinterpret_cast<const uint4*>(a_row[j] + g0 * 4));
+              a[j][0] = v.x; a[j][1] = v.y; a[j][2] = v.z; a[j][3] = v.w;
+            } else {
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                a[j][q] = q < ng ? __ldcg(reinterpret_cast<const uint32_t*>(a_row[j] + (g0 + q) * 4)) : 0u;
+            }
+          } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) a[j][q] = 0u;       // rows past the block: unused accumulator lanes
           }
         }
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          cp_async_4(dB + j * 4, b_sf_base + (size_t)(b_row0 + lane + 32 * j) * kstride + kb * 4);
-        if (two_sfb) {
+        for (int j = 0; j < 8; ++j) {
+          if (b_vec && ng == 4) {
+            const uint4 v = __ldg(reinterpret_cast<const uint4*>(b_row[j] + g0 * 4));
+            b[j][0] = v.x; b[j][1] = v.y; b[j][2] = v.z; b[j][3] = v.w;
+          } else {
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            cp_async_4(dB + 512 + j * 4, b_sf_base + (size_t)(b_row1 + lane + 32 * j) * kstride + kb * 4);
+            for (int q = 0; q < 4; ++q)
+              b[j][q] = q < ng ? __ldg(reinterpret_cast<const uint32_t*>(b_row[j] + (g0 + q) * 4)) : 0u;
+          }
         }
-        cp_async_commit();
-        ++gathered;
-        if (gathered - armed == kSfLag) release_oldest(false);
-        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          if (q >= ng) break;
+          bool w = true;
+          if (lane == 0) w = mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, ctrl, to, (kSiteEmpty << 24) | tag);
+          w = __shfl_sync(0xffffffffu, w, 0);
+          if (!w) { ok = false; break; }
+          uint4* dA = reinterpret_cast<uint4*>(sSFA + stage * kSFABytes) + lane;
+          uint4* dB = reinterpret_cast<uint4*>(sSFB + stage * kSFBBytes) + lane;
+          *dA = make_uint4(a[0][q], a[1][q], a[2][q], a[3][q]);
+          dB[0] = make_uint4(b[0][q], b[1][q], b[2][q], b[3][q]);
+          dB[32] = make_uint4(b[4][q], b[5][q], b[6][q], b[7][q]);
+          fence_proxy_async_shared();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&full[stage]));
+          ++armed;
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
       }
       if (!ok) break;
     }
-    while (armed < gathered) release_oldest(true);
     if (lane == 0) s_misc[4] = armed;
   } else {
     // ---------------- epilogue: warp w reads TMEM lanes 32q..32q+31 (token rows), q = w % 4;
