@@ -56,10 +56,16 @@ constexpr uint32_t kSFSetCols = 12;                 // SFA: +0..3, SFB: +4..11
 // factors, tcgen05.mma kind::f16, bf16 L1 activations.  Its K stage is 64
 // elements, so rows stay 128 bytes and every shared-memory footprint and box
 // byte count of a stage is that of the FP8 x FP4 layer.
-template <int kARows_, int kStages_, bool kXpose_, bool kBf16_>
+//
+// kSub: K sub-stages (128 wide each, or 64 for bf16) per ring slot.  A slot is
+// one full/empty barrier round trip; two sub-stages per slot halve the round
+// trips, waits and commits per weight byte at the same bytes in flight.
+template <int kARows_, int kStages_, bool kXpose_, bool kBf16_, int kSub_ = 1>
 struct Variant {
   static constexpr int kARows = kARows_;
-  static constexpr int kStages = kStages_;
+  static constexpr int kStages = kStages_;            // ring slots
+  static constexpr int kSub = kSub_;                   // sub-stages per slot
+  static_assert(kSub == 1 || kSub == 2, "sub-stages per slot");
   static constexpr bool kXpose = kXpose_;
   static constexpr bool kBf16 = kBf16_;
   static constexpr int kKStage = kBf16 ? kBlockK / 2 : kBlockK;     // K elements per stage
@@ -70,19 +76,19 @@ struct Variant {
   // L2 epilogue stores whole 64-byte row segments instead of 16-byte pieces of
   // 32 different rows.
   static constexpr int kXposeBytes = kXpose ? kEpiWarps * 32 * 16 * 4 : 0;
-  static constexpr int kSmemBytes = kStages * kStageBytes + kXposeBytes + kBarBytes + 1024 /*align*/;
+  static constexpr int kSmemBytes = kStages * kSub * kStageBytes + kXposeBytes + kBarBytes + 1024 /*align*/;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
   static_assert(kABytes % 1024 == 0 && kBBytes % 1024 == 0, "SW128 tiles need 1 KB alignment");
   static_assert(kARows % 16 == 0 && kARows <= kTileM, "token rows per stage");
   // barriers (2 per stage, 3 accumulator/drain, 2 per tile-ring slot), misc words, votes, tile ring
   static_assert((2 * kStages + 3 + 2 * kTileRing) * 8 + 8 * 4 + 2 * kEpiWarps * 4 + kTileRing * 9 * 4 <= kBarBytes,
                 "barrier region");
-  static_assert(kSFCol0 + kStages * kSFSetCols <= kTmemCols, "scale-factor sets fit TMEM");
-  // the MMA's 128-row A window of the last stage stays inside the allocation
-  static_assert((kStages - 1) * kABytes + kTileM * kBlockK <= kStages * kStageBytes, "A window");
+  static_assert(kSFCol0 + kStages * kSub * kSFSetCols <= kTmemCols, "scale-factor sets fit TMEM");
+  // the MMA's 128-row A window of the last sub-stage stays inside the allocation
+  static_assert((kStages * kSub - 1) * kABytes + kTileM * kBlockK <= kStages * kSub * kStageBytes, "A window");
 };
 using WideVariant = Variant<128, 4, true, false>;
-using ThinVariant = Variant<32, 6, false, false>;
+using ThinVariant = Variant<32, 3, false, false, 2>;
 using Bf16WideVariant = Variant<128, 4, true, true>;
 using Bf16ThinVariant = Variant<32, 6, false, true>;
 enum VariantId : int {

@@ -168,16 +168,18 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
                const __grid_constant__ CUtensorMap tm_xs16, const __grid_constant__ CUtensorMap tm_xs128,
                const __grid_constant__ CUtensorMap tm_l1a16, const __grid_constant__ CUtensorMap tm_l1a128,
                const __grid_constant__ ForwardParams p) {
-  constexpr int kStages = V::kStages;
+  constexpr int kStages = V::kStages;     // ring slots
+  constexpr int kSub = V::kSub;           // sub-stages per slot; sub-stage buffers are indexed slot * kSub + u
   constexpr int kABytes = V::kABytes;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sA = sm;                                   // [kStages] token rows
-  uint8_t* sB = sA + kStages * kABytes;               // [kStages] weight rows
-  uint8_t* sSFA = sB + kStages * kBBytes;             // [kStages] token scale atom
-  uint8_t* sSFB = sSFA + kStages * kSFABytes;         // [kStages] two weight scale atoms
-  float* sX = reinterpret_cast<float*>(sSFB + kStages * kSFBBytes);   // [kEpiWarps] transpose buffers
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sSFB + kStages * kSFBBytes + V::kXposeBytes);
+  constexpr int kSubs = kStages * kSub;
+  uint8_t* sA = sm;                                   // [kSubs] token rows
+  uint8_t* sB = sA + kSubs * kABytes;                 // [kSubs] weight rows
+  uint8_t* sSFA = sB + kSubs * kBBytes;               // [kSubs] token scale atom
+  uint8_t* sSFB = sSFA + kSubs * kSFABytes;           // [kSubs] two weight scale atoms
+  float* sX = reinterpret_cast<float*>(sSFB + kSubs * kSFBBytes);   // [kEpiWarps] transpose buffers
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sSFB + kSubs * kSFBBytes + V::kXposeBytes);
   uint64_t* full = bars;                     // [kStages] both producers' TMA bytes + the scale loader's atoms
   uint64_t* empty = bars + kStages;          // [kStages] MMAs reading the stage are done
   uint64_t* tfull = bars + 2 * kStages;      // accumulator ready
@@ -369,18 +371,22 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
                                                 : (full_box ? &tm_l1a128 : &tm_l1a16);
         const int b_row = ti.layer == 1 ? ti.e * 2 * p.I + ti.nb * kL1Feat + pid * p.I
                                         : ti.e * p.H + ti.nb * kTileN + pid * 128;
-        for (int kb = 0; kb < ti.ks; ++kb) {
+        for (int kk0 = 0; kk0 < ti.ks; kk0 += kSub) {
+          const int nsub = min(kSub, ti.ks - kk0);
           if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, ctrl, to, (kSiteEmpty << 24) | tag)) { ok = false; break; }
           const uint32_t fb = smem_u32(&full[stage]);
-          mbar_arrive_expect_tx(fb, bytes);
-          const uint32_t a_dst = smem_u32(sA + stage * kABytes);
-          const uint32_t b_dst = smem_u32(sB + stage * kBBytes) + (uint32_t)(pid * 128 * kBlockK);
-          const int kx = kb * V::kKStage;
-          if (my_b) tma_load_2d(b_dst, tm_b, fb, kx, b_row);
-          if (full_box) {
-            if (pid == 0) tma_load_2d(a_dst, tm_a, fb, kx, ti.r0);
-          } else {
-            for (int j = pid; j < nbox; j += 2) tma_load_2d(a_dst + j * 16 * kBlockK, tm_a, fb, kx, ti.r0 + 16 * j);
+          mbar_arrive_expect_tx(fb, bytes * (uint32_t)nsub);
+          for (int u = 0; u < nsub; ++u) {
+            const int gs = stage * kSub + u;
+            const uint32_t a_dst = smem_u32(sA + gs * kABytes);
+            const uint32_t b_dst = smem_u32(sB + gs * kBBytes) + (uint32_t)(pid * 128 * kBlockK);
+            const int kx = (kk0 + u) * V::kKStage;
+            if (my_b) tma_load_2d(b_dst, tm_b, fb, kx, b_row);
+            if (full_box) {
+              if (pid == 0) tma_load_2d(a_dst, tm_a, fb, kx, ti.r0);
+            } else {
+              for (int j = pid; j < nbox; j += 2) tma_load_2d(a_dst + j * 16 * kBlockK, tm_a, fb, kx, ti.r0 + 16 * j);
+            }
           }
           ++issued;
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
@@ -413,26 +419,30 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
         const uint32_t id3 = id0 | (3u << 4) | (3u << 29);
         const bool two_sfb = ti.n > 128;
         const uint32_t idb = idesc_bf16((uint32_t)ti.n);
-        for (int kb = 0; kb < ti.ks; ++kb) {
+        for (int kk0 = 0; kk0 < ti.ks; kk0 += kSub) {
+          const int nsub = min(kSub, ti.ks - kk0);
           if (!mbar_wait(full0 + stage * 8u, phase, ctrl, to, (kSiteFull << 24) | tag)) { ok = false; break; }
-          const uint32_t so = stage;
-          const uint64_t ad = a_desc0 + (uint64_t)(so * (uint32_t)(kABytes >> 4));
-          const uint64_t bd = b_desc0 + (uint64_t)(so * (uint32_t)(kBBytes >> 4));
-          if constexpr (V::kBf16) {
-            tc_mma_f16(tmem, ad, bd, idb, kb != 0 ? 1u : 0u);            // K = 16 each: +32 bytes
-            tc_mma_f16(tmem, ad + 2, bd + 2, idb, 1u);
-            tc_mma_f16(tmem, ad + 4, bd + 4, idb, 1u);
-            tc_mma_f16(tmem, ad + 6, bd + 6, idb, 1u);
-          } else {
-            const uint64_t sfb_d = sfb_desc0 + (uint64_t)(so * (uint32_t)(kSFBBytes >> 4));
-            const uint32_t sfa_t = tmem + kSFCol0 + so * kSFSetCols, sfb_t = sfa_t + 4;
-            tc_cp_sf(sfa_t, sfa_desc0 + (uint64_t)(so * (uint32_t)(kSFABytes >> 4)));
-            tc_cp_sf(sfb_t, sfb_d);
-            if (two_sfb) tc_cp_sf(sfb_t + 4, sfb_d + (512 >> 4));
-            tc_mma_mx(tmem, ad, bd, id0, sfa_t, sfb_t, kb != 0 ? 1u : 0u);
-            tc_mma_mx_acc(tmem, ad + 2, bd + 2, id1, sfa_t, sfb_t);     // K = 32 each: +32 bytes
-            tc_mma_mx_acc(tmem, ad + 4, bd + 4, id2, sfa_t, sfb_t);
-            tc_mma_mx_acc(tmem, ad + 6, bd + 6, id3, sfa_t, sfb_t);
+          for (int u = 0; u < nsub; ++u) {
+            const uint32_t so = (uint32_t)(stage * kSub + u);
+            const uint32_t acc0 = (kk0 + u) != 0 ? 1u : 0u;
+            const uint64_t ad = a_desc0 + (uint64_t)(so * (uint32_t)(kABytes >> 4));
+            const uint64_t bd = b_desc0 + (uint64_t)(so * (uint32_t)(kBBytes >> 4));
+            if constexpr (V::kBf16) {
+              tc_mma_f16(tmem, ad, bd, idb, acc0);                       // K = 16 each: +32 bytes
+              tc_mma_f16(tmem, ad + 2, bd + 2, idb, 1u);
+              tc_mma_f16(tmem, ad + 4, bd + 4, idb, 1u);
+              tc_mma_f16(tmem, ad + 6, bd + 6, idb, 1u);
+            } else {
+              const uint64_t sfb_d = sfb_desc0 + (uint64_t)(so * (uint32_t)(kSFBBytes >> 4));
+              const uint32_t sfa_t = tmem + kSFCol0 + so * kSFSetCols, sfb_t = sfa_t + 4;
+              tc_cp_sf(sfa_t, sfa_desc0 + (uint64_t)(so * (uint32_t)(kSFABytes >> 4)));
+              tc_cp_sf(sfb_t, sfb_d);
+              if (two_sfb) tc_cp_sf(sfb_t + 4, sfb_d + (512 >> 4));
+              tc_mma_mx(tmem, ad, bd, id0, sfa_t, sfb_t, acc0);
+              tc_mma_mx_acc(tmem, ad + 2, bd + 2, id1, sfa_t, sfb_t);   // K = 32 each: +32 bytes
+              tc_mma_mx_acc(tmem, ad + 4, bd + 4, id2, sfa_t, sfb_t);
+              tc_mma_mx_acc(tmem, ad + 6, bd + 6, id3, sfa_t, sfb_t);
+            }
           }
           tc_commit(empty0 + stage * 8u);
           ++consumed;
@@ -534,17 +544,23 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
           }
         }
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < 4; q += kSub) {                  // one ring slot: K stages g0 + q .. + kSub - 1
           if (q >= ng) break;
           bool w = true;
           if (lane == 0) w = mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, ctrl, to, (kSiteEmpty << 24) | tag);
           w = __shfl_sync(0xffffffffu, w, 0);
           if (!w) { ok = false; break; }
-          uint4* dA = reinterpret_cast<uint4*>(sSFA + stage * kSFABytes) + lane;
-          uint4* dB = reinterpret_cast<uint4*>(sSFB + stage * kSFBBytes) + lane;
-          *dA = make_uint4(a[0][q], a[1][q], a[2][q], a[3][q]);
-          dB[0] = make_uint4(b[0][q], b[1][q], b[2][q], b[3][q]);
-          dB[32] = make_uint4(b[4][q], b[5][q], b[6][q], b[7][q]);
+#pragma unroll
+          for (int u = 0; u < kSub; ++u) {
+            if (q + u < ng) {
+              const int gs = stage * kSub + u;
+              uint4* dA = reinterpret_cast<uint4*>(sSFA + gs * kSFABytes) + lane;
+              uint4* dB = reinterpret_cast<uint4*>(sSFB + gs * kSFBBytes) + lane;
+              *dA = make_uint4(a[0][q + u], a[1][q + u], a[2][q + u], a[3][q + u]);
+              dB[0] = make_uint4(b[0][q + u], b[1][q + u], b[2][q + u], b[3][q + u]);
+              dB[32] = make_uint4(b[4][q + u], b[5][q + u], b[6][q + u], b[7][q + u]);
+            }
+          }
           fence_proxy_async_shared();
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&full[stage]));
