@@ -19,8 +19,11 @@ from layer_inputs import (ExpertCache, GpuTokens, GpuWeights, bf16_to_np, close_
 pytestmark = pytest.mark.gpu
 
 CASES = [
+    # wide kernel variant (more than 16 assignments per expert on average)
     synth.Config("graph-balanced", T=256, H=512, I=256, E=16, k=4, clamp=7.0, seed=20),
     synth.Config("graph-skewed", T=200, H=512, I=256, E=96, k=8, clamp=0.0, skew=True, seed=21),
+    # thin variant (decode-shaped: ~4 assignments per expert; odd K-stage count per tile)
+    synth.Config("graph-decode", T=64, H=384, I=384, E=64, k=4, clamp=7.0, seed=22),
 ]
 
 
