@@ -57,8 +57,8 @@ typedef enum {
   MM_ERR_UNSUPPORTED_SHAPE = -2,   /* dimensions outside the supported envelope       */
   MM_ERR_WORKSPACE_TOO_SMALL = -3, /* workspace_bytes < mm_workspace_size(...)        */
   MM_ERR_CUDA = -4,                /* a CUDA runtime/driver call failed               */
-  MM_ERR_TIMEOUT = -5,             /* a device wait (grid barrier, readiness counter,
-                                      pipeline barrier) ran past its time limit       */
+  MM_ERR_TIMEOUT = -5,             /* a device wait (readiness counter, pipeline
+                                      barrier, tile ring) ran past its time limit     */
   MM_ERR_BAD_INDEX = -6,           /* topk_idx outside [-1, experts)                  */
   MM_ERR_BOUNDS = -7,              /* reserved for checked builds                     */
   MM_ERR_NO_DEVICE = -8            /* no usable sm_103 device                         */
@@ -116,8 +116,8 @@ size_t mm_workspace_size(int max_tokens, int experts, int topk, int hidden, int 
  *             one workspace must not be used by two launches that overlap.
  *   stream    the stream to enqueue on.
  *
- * Enqueues two kernels (routing, then the persistent layer kernel) and
- * returns.  T = 0 returns MM_OK without launching.  Device-side errors land in
+ * Enqueues three kernels (routing, the persistent layer kernel, then the
+ * top-k combine) and returns.  T = 0 returns MM_OK without launching.  Device-side errors land in
  * the workspace status (mm_get_status); the next mm_forward resets it.  Every
  * device wait is bounded by mm_set_wait_timeout_ns; a wait that runs out sets
  * MM_ERR_TIMEOUT and the kernel returns instead of hanging.  The call makes

@@ -99,14 +99,14 @@ enum VariantId : int {
 // ----------------------------------------------------------------- control block
 // 32-bit words at the head of the workspace.
 enum CtrlWord : int {
-  kStatus = 0, kErrSm = 1, kErrInfo = 2, kAbort = 3, kGridBar = 4, kSiteMask = 5, kNextTile = 6, kCtrlWords = 64
+  kStatus = 0, kErrSm = 1, kErrInfo = 2, kAbort = 3, kUnused4 = 4, kSiteMask = 5, kNextTile = 6, kCtrlWords = 64
 };
 
 
 // Wait sites recorded in the error info word (site << 24 | tile & 0xFFFFFF).
 enum WaitSite : uint32_t {
   kSiteFull = 1, kSiteEmpty = 2, kSiteTmemFull = 3, kSiteTmemEmpty = 4,
-  kSiteArrival = 5, kSiteL1Done = 6, kSiteGridBar = 7, kSiteDrain = 8, kSiteFullSf = 9, kSiteTileRing = 10
+  kSiteArrival = 5, kSiteL1Done = 6, kSiteUnused7 = 7, kSiteDrain = 8, kSiteFullSf = 9, kSiteTileRing = 10
 };
 
 // ----------------------------------------------------------------- workspace

@@ -2,7 +2,10 @@
 //
 // One CTA per SM (grid sized by the host from the SM count minus a reserve,
 // rounded down to even -- sglang PR #36657 "[Blackwell] Reserve SMs for
-// DeepGEMM MegaMoE grid barriers", sections Root cause and Fix).  Phases:
+// DeepGEMM MegaMoE grid barriers", sections Root cause and Fix).  The
+// dispatch below is a static grid-stride loop, so the layer is only sure to
+// progress when every CTA is resident at once; the reserve keeps that true
+// while another stream holds a few SMs.  Phases:
 //
 //  0. dispatch: every warp copies expert-sorted token rows (and their UE8M0
 //     scales) into the workspace and bumps that expert's arrival counter with
@@ -32,8 +35,12 @@
 //     weight and writes fp32 rows indexed by the flat assignment (fp32, not
 //     bf16: when a token's k contributions cancel, a bf16 rounding of each one
 //     is large next to their sum).
-//  2. whole-grid software barrier, then the combine: y[t] = bf16(sum_j of the
-//     weighted rows t*k + j, in ascending j).
+// The combine, y[t] = bf16(sum_j of the weighted rows t*k + j, in ascending
+// j), is a second, non-persistent kernel on the same stream (combine_kernel):
+// the kernel boundary orders every L2 row before it, so the layer kernel has
+// no whole-grid barrier, and the combine runs on every SM at HBM rate.  (The
+// pages' kernel synchronises its grid after the epilogue and combines in the
+// same kernel.)
 //
 // Every wait is bounded (global timer + abort flag): a wait that runs out
 // records MM_ERR_TIMEOUT with the SM and the wait site, raises the abort flag,
@@ -187,7 +194,7 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
   uint64_t* drain = tempty + 1;              // final MMA drain
   uint64_t* tile_full = drain + 1;           // [kTileRing] tile index published
   uint64_t* tile_empty = tile_full + kTileRing;   // [kTileRing] read by every consumer role
-  // tmem base, stages consumed (MMA), stages issued (producer 0), combine off, stages armed (scale
+  // tmem base, stages consumed (MMA), stages issued (producer 0), (unused), stages armed (scale
   // loader), stages issued (producer 1)
   uint32_t* s_misc = reinterpret_cast<uint32_t*>(tile_empty + kTileRing);
   int32_t* s_vote = reinterpret_cast<int32_t*>(s_misc + 8);    // epilogue votes [2][kEpiWarps]
@@ -777,27 +784,24 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
     tc_fence_after();
     tc_dealloc(tmem, kTmemCols);
   }
+}
 
-  // ------------------------------------------------------------ 2. grid barrier + combine
-  if (threadIdx.x == 0) {
-    __threadfence();
-    bool fine = ld_volatile(&ctrl[kAbort]) == 0u;
-    if (fine) {
-      red_release_add(&ctrl[kGridBar], 1u);
-      fine = counter_wait(&ctrl[kGridBar], gridDim.x, ctrl, to, kSiteGridBar << 24);
-    }
-    s_misc[3] = fine ? 0u : 1u;
-  }
-  __syncthreads();
-  if (s_misc[3] != 0u) return;
-
-  // work item = (token, up to 1024 outputs): 128 uint4 chunks of 8 bf16, 4 per lane
+// The top-k weighted combine, one warp per (token, up to 1024 outputs): 128
+// uint4 chunks of 8 bf16, 4 per lane.  y[t, c] = bf16_RNE(sum over the token's
+// valid slots j, ascending, of stage[t*k + j, c]), summed in fp32 from zero; a
+// token routed nowhere gets a zero row.  Nothing is combined after an error.
+__global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ ForwardParams p) {
+  const uint32_t* ctrl = reinterpret_cast<const uint32_t*>(p.ws + p.L.ctrl);
+  if (ld_volatile(&ctrl[kStatus]) != 0u) return;
+  const float* stage_out = reinterpret_cast<const float*>(p.ws + p.L.stage);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int H = p.H, k = p.k;
   const int nchunk = H / 8;
   const int per_item = 128;
   const int items_per_token = (nchunk + per_item - 1) / per_item;
   const int nitems = p.T * items_per_token;
-  for (int it = blockIdx.x * (kThreads / 32) + warp; it < nitems; it += gridDim.x * (kThreads / 32)) {
+  const int wpb = blockDim.x >> 5;
+  for (int it = blockIdx.x * wpb + warp; it < nitems; it += gridDim.x * wpb) {
     const int t = it / items_per_token;
     const int c_beg = (it - t * items_per_token) * per_item;
     const int c_end = min(c_beg + per_item, nchunk);
@@ -814,9 +818,9 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
         float4 a[8], b[8];
 #pragma unroll
         for (int jj = 0; jj < 8; ++jj) {
-          if (j0 + jj < k) {
-            a[jj] = __ldcg(rows + (size_t)(j0 + jj) * (H / 4) + 2 * c);
-            b[jj] = __ldcg(rows + (size_t)(j0 + jj) * (H / 4) + 2 * c + 1);
+          if (j0 + jj < k && ((valid >> (j0 + jj)) & 1u)) {
+            a[jj] = __ldcs(rows + (size_t)(j0 + jj) * (H / 4) + 2 * c);
+            b[jj] = __ldcs(rows + (size_t)(j0 + jj) * (H / 4) + 2 * c + 1);
           }
         }
 #pragma unroll
@@ -866,13 +870,22 @@ static cudaError_t launch_one(int grid, cudaStream_t stream, const CUtensorMap* 
 }
 
 // maps: W1, W2, dispatched tokens (16- and 128-row boxes), L1 activations (16- and 128-row boxes)
+// The layer kernel, then the combine kernel on the same stream (8 CTAs of 256
+// threads per layer CTA: a full SM's worth of warps on each of those SMs).
 cudaError_t layer_launch(int variant, int grid, cudaStream_t stream, const CUtensorMap* maps, const ForwardParams& p) {
+  cudaError_t e;
   switch (variant) {
-    case kVariantThin: return launch_one<ThinVariant>(grid, stream, maps, p);
-    case kVariantBf16Wide: return launch_one<Bf16WideVariant>(grid, stream, maps, p);
-    case kVariantBf16Thin: return launch_one<Bf16ThinVariant>(grid, stream, maps, p);
-    default: return launch_one<WideVariant>(grid, stream, maps, p);
+    case kVariantThin: e = launch_one<ThinVariant>(grid, stream, maps, p); break;
+    case kVariantBf16Wide: e = launch_one<Bf16WideVariant>(grid, stream, maps, p); break;
+    case kVariantBf16Thin: e = launch_one<Bf16ThinVariant>(grid, stream, maps, p); break;
+    default: e = launch_one<WideVariant>(grid, stream, maps, p); break;
   }
+  if (e != cudaSuccess) return e;
+  const long long items = (long long)p.T * ((p.H / 8 + 127) / 128);
+  const long long want = (items + 7) / 8;
+  const int blocks = (int)std::max(1ll, std::min(want, 8ll * grid));
+  combine_kernel<<<blocks, 256, 0, stream>>>(p);
+  return cudaGetLastError();
 }
 
 }  // namespace mm

@@ -61,7 +61,7 @@ __global__ void __launch_bounds__(1024, 1) route_kernel(const RouteParams p) {
   int32_t* perm = reinterpret_cast<int32_t*>(p.ws + p.L.perm);
   int32_t* inv = reinterpret_cast<int32_t*>(p.ws + p.L.inv);
 
-  // -- reset: status, abort flag, grid barrier, readiness counters
+  // -- reset: status, abort flag, tile counter, readiness counters
   for (int i = tid; i < kCtrlWords; i += blockDim.x) ctrl[i] = 0u;
   for (int i = tid; i < E; i += blockDim.x) { arrival[i] = 0u; l1_done[i] = 0u; }
   for (int i = tid; i < 32 * E; i += blockDim.x) hist[i] = 0;
