@@ -41,7 +41,7 @@ UNIT = "tokens/s"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 FP8_PER_BF16 = 2.0          # nominal dense rate ratio (4.5 vs 2.25 PFLOP/s)
-HBM_TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "megamoe_kernel_decode.traffic.json")
+HBM_TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "megamoe_combine_decode.traffic.json")
 
 
 # ------------------------------------------------------------------ helpers
