@@ -349,7 +349,7 @@ def run_ours(args, rank, world, local_rank):
         "tokens_per_s": tokens_per_s, "ms": ms, "route_ms": route_ms, "roofline": roofline,
         "e2e": {"value": round(e2e_tps, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
-        "clocks": clk.summary(), "wall_s": t_wall, "gpu_launches": 3 * args.steps, "step_ms": pct,
+        "clocks": clk.summary(), "wall_s": t_wall, "gpu_launches": ((1 if T * k <= 2048 else 3) + 2) * args.steps, "step_ms": pct,
         "cfg": cfg, "touched": touched,
     }
 

@@ -116,8 +116,8 @@ size_t mm_workspace_size(int max_tokens, int experts, int topk, int hidden, int 
  *             one workspace must not be used by two launches that overlap.
  *   stream    the stream to enqueue on.
  *
- * Enqueues three kernels (routing, the persistent layer kernel, then the
- * top-k combine) and returns.  T = 0 returns MM_OK without launching.  Device-side errors land in
+ * Enqueues the routing (one kernel, or three above 2048 assignments), the
+ * persistent layer kernel, then the top-k combine, and returns.  T = 0 returns MM_OK without launching.  Device-side errors land in
  * the workspace status (mm_get_status); the next mm_forward resets it.  Every
  * device wait is bounded by mm_set_wait_timeout_ns; a wait that runs out sets
  * MM_ERR_TIMEOUT and the kernel returns instead of hanging.  The call makes
@@ -220,10 +220,11 @@ unsigned long long mm_get_wait_timeout_ns(void);
 int mm_get_status(const void* workspace, mm_stream_t stream, int* sm, int* info);
 
 /*
- * mm_route -- runs only the routing kernel of mm_forward (reset, expert
- * histogram, prefix scan, stable permutation) into `workspace` ([P3] Phase 2
- * entry: expert count, source token-topk index write).  Same argument rules
- * as mm_forward.  Test hook.
+ * mm_route -- runs only the routing of mm_forward (reset, expert histogram,
+ * prefix scan, stable permutation) into `workspace` ([P3] Phase 2 entry:
+ * expert count, source token-topk index write): one kernel up to 2048
+ * assignments, else three (per-chunk counts, scan, scatter).  Same argument
+ * rules as mm_forward.  Test hook.
  */
 int mm_route(int num_tokens, int experts, int topk, int hidden, int inter,
              const int32_t* topk_idx, void* workspace, size_t workspace_bytes,
@@ -249,6 +250,8 @@ int mm_read_routing(int num_tokens, int experts, int topk, int hidden, int inter
  *   9 dispatched x_sf [T*k, H/32]  10 l1_acts [T*k, I] (E4M3, slot order)
  *  11 l1_acts_sf [T*k, I/32]        12 weighted L2 outputs, fp32 [T*k, H]
  *     indexed by the flat assignment t*k+j
+ *  13 routing chunk table: int32 [E][C] then [C], C = 1 up to 2048
+ *     assignments, else min(ceil(T*k / 1024), 128) chunks
  * Returns MM_OK, or MM_ERR_INVALID_ARG for an unknown region or shape.
  */
 int mm_workspace_region(int which, int num_tokens, int experts, int topk, int hidden,

@@ -11,6 +11,9 @@
 
 namespace mm {
 __global__ void route_kernel(const RouteParams p);
+__global__ void route_count_kernel(const RouteParams p);
+__global__ void route_scan_kernel(const RouteParams p);
+__global__ void route_scatter_kernel(const RouteParams p);
 int layer_max_rows(int variant);
 cudaError_t layer_prepare(int variant, int* ctas_per_sm);
 cudaError_t layer_launch(int variant, int grid, cudaStream_t stream, const CUtensorMap* maps, const ForwardParams& p);
@@ -98,7 +101,11 @@ int device_state(int* dev_out, DevState** st_out) {
       }
       g_encode = reinterpret_cast<EncodeTiledFn>(fn);
     }
-    if (cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 32 * 1024 * 4) != cudaSuccess) {
+    if (cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 32 * 1024 * 4) != cudaSuccess ||
+        cudaFuncSetAttribute(route_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 32 * 1024 * 4) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(route_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 32 * 1024 * 4) !=
+            cudaSuccess) {
       cudaGetLastError();
       return MM_ERR_CUDA;
     }
@@ -133,11 +140,20 @@ int encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t
 int launch_route(int T, int E, int k, const int32_t* topk_idx, uint8_t* ws, const Layout& L, cudaStream_t st) {
   RouteParams rp;
   rp.T = T; rp.E = E; rp.k = k; rp.A = T * k;
+  rp.C = route_ctas(rp.A);
+  rp.chunk = (rp.A + rp.C - 1) / rp.C;
   rp.max_n = layer_max_rows(pick_variant((long long)T * k, E, false));   // the same rows for both layers
   rp.topk_idx = topk_idx;
   rp.ws = ws;
   rp.L = L;
-  route_kernel<<<1, 1024, (size_t)32 * E * 4, st>>>(rp);
+  const size_t smem = (size_t)32 * E * 4;
+  if (rp.C == 1) {
+    route_kernel<<<1, 1024, smem, st>>>(rp);
+  } else {
+    route_count_kernel<<<rp.C, 1024, smem, st>>>(rp);
+    route_scan_kernel<<<1, 1024, 0, st>>>(rp);
+    route_scatter_kernel<<<rp.C, 1024, smem, st>>>(rp);
+  }
   if (cudaGetLastError() != cudaSuccess) return MM_ERR_CUDA;
   return MM_OK;
 }
@@ -355,12 +371,14 @@ int mm_workspace_region(int which, int num_tokens, int experts, int topk, int hi
   if (check_shape(num_tokens, experts, topk, hidden, inter) != MM_OK) return MM_ERR_INVALID_ARG;
   const Layout L = make_layout(num_tokens, experts, topk, hidden, inter);
   const size_t starts[14] = {L.ctrl, L.counts, L.offsets, L.items, L.arrival, L.l1_done, L.perm, L.inv,
-                             L.xs, L.xs_sf, L.l1a, L.l1a_sf, L.stage, L.total};
-  if (which < 0 || which > 12) return MM_ERR_INVALID_ARG;
+                             L.xs, L.xs_sf, L.l1a, L.l1a_sf, L.stage, L.rhist};
+  if (which < 0 || which > 13) return MM_ERR_INVALID_ARG;
   const size_t A = (size_t)num_tokens * topk;
-  const size_t exact[13] = {4 * (size_t)kCtrlWords, 4 * (size_t)experts, 4 * (size_t)(experts + 1),
+  const size_t C = (size_t)route_ctas((long long)A);
+  const size_t exact[14] = {4 * (size_t)kCtrlWords, 4 * (size_t)experts, 4 * (size_t)(experts + 1),
                             4 * (size_t)(experts + 1), 4 * (size_t)experts, 4 * (size_t)experts, 4 * A, 4 * A,
-                            A * hidden, A * (hidden / 32), A * inter, A * (inter / 32), A * hidden * 4};
+                            A * hidden, A * (hidden / 32), A * inter, A * (inter / 32), A * hidden * 4,
+                            4 * (size_t)experts * C + 4 * C};
   if (offset) *offset = starts[which];
   if (bytes) *bytes = exact[which];
   return MM_OK;

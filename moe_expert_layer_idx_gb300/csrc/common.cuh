@@ -112,10 +112,22 @@ enum WaitSite : uint32_t {
 // ----------------------------------------------------------------- workspace
 struct Layout {
   size_t ctrl, counts, offsets, items, arrival, l1_done, perm, inv;
-  size_t xs, xs_sf, l1a, l1a_sf, stage, total;
+  size_t xs, xs_sf, l1a, l1a_sf, stage, rhist, total;
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Routing CTAs: one 1024-thread CTA handles up to 2048 assignments alone;
+// larger batches are split into contiguous chunks of about 1024 assignments
+// (at most 128 chunks), counted, scanned and scattered by three kernels.
+constexpr int kRouteChunk = 1024;
+constexpr int kMaxRouteCtas = 128;     // the scan kernel takes an expert's chunk counts in 4 steps of 32
+static_assert(kMaxRouteCtas <= 128, "route_scan_kernel scans at most 128 chunks");
+__host__ __device__ inline int route_ctas(long long A) {
+  if (A <= 2 * kRouteChunk) return 1;
+  const long long c = (A + kRouteChunk - 1) / kRouteChunk;
+  return c < kMaxRouteCtas ? (int)c : kMaxRouteCtas;
+}
 
 // esz: bytes per activation element (1: E4M3 codes with UE8M0 scales; 2: bf16,
 // whose scale regions stay unused).
@@ -136,6 +148,9 @@ __host__ __device__ inline Layout make_layout(long long T, int E, int k, int H, 
   L.l1a = o;      o = align256(o + A * (size_t)I * esz);
   L.l1a_sf = o;   o = align256(o + A * (size_t)(I / 32));
   L.stage = o;    o = align256(o + A * (size_t)H * 4);
+  // per-chunk expert counts, then base slots, [E][C] int32, and one bad-index word per chunk
+  const size_t C = (size_t)route_ctas((long long)A);
+  L.rhist = o;    o = align256(o + 4 * (size_t)E * C + 4 * C);
   L.total = o;
   return L;
 }
@@ -169,6 +184,7 @@ struct ForwardParams {
 struct RouteParams {
   int T, E, k;
   int A;
+  int C, chunk;                // routing CTAs and the assignments each one owns
   int max_n;                   // largest token block of the layer kernel
   const int32_t* topk_idx;
   uint8_t* ws;

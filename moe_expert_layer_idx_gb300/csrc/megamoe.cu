@@ -307,30 +307,48 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
     const int H = p.H;
     constexpr int esz = V::kBf16 ? 2 : 1;          // bytes per activation element
     const int nvec = H * esz / 16, nsf = H / 128;
-    for (int s = blockIdx.x * (kThreads / 32) + warp; s < nvalid; s += gridDim.x * (kThreads / 32)) {
-      const int f = __ldg(perm + s);
-      const int t = f / p.k;
-      const int e = __ldg(p.topk_idx + f);
-      const uint4* src = reinterpret_cast<const uint4*>(p.x + (size_t)t * H * esz);
-      uint4* dst = reinterpret_cast<uint4*>(xs + (size_t)s * H * esz);
-      for (int c0 = lane; c0 < nvec; c0 += 32 * 8) {       // 8 independent loads in flight per lane
-        uint4 v[8];
+    // A warp copies its slots s0, s0 + G, ... in batches of kBatch: the batch's
+    // perm and expert entries are loaded together, each row with up to 16
+    // loads in flight per lane, and one fence covers the whole batch before
+    // its arrival counts are released.
+    constexpr int kBatch = 4;
+    const int G = gridDim.x * (kThreads / 32);
+    for (int s0 = blockIdx.x * (kThreads / 32) + warp; s0 < nvalid; s0 += kBatch * G) {
+      int fs[kBatch], es[kBatch];
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-          if (c0 + 32 * i < nvec) v[i] = __ldg(src + c0 + 32 * i);
+      for (int u = 0; u < kBatch; ++u) fs[u] = s0 + u * G < nvalid ? __ldg(perm + s0 + u * G) : -1;
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-          if (c0 + 32 * i < nvec) dst[c0 + 32 * i] = v[i];
-      }
-      if (!V::kBf16) {
-        const uint32_t* ssf = reinterpret_cast<const uint32_t*>(p.x_sf + (size_t)t * (H / 32));
-        uint32_t* dsf = reinterpret_cast<uint32_t*>(xs_sf + (size_t)s * (H / 32));
-        for (int c = lane; c < nsf; c += 32) dsf[c] = __ldg(ssf + c);
+      for (int u = 0; u < kBatch; ++u) es[u] = fs[u] >= 0 ? __ldg(p.topk_idx + fs[u]) : -1;
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        if (fs[u] < 0) continue;                      // warp-uniform
+        const int s = s0 + u * G;
+        const int t = fs[u] / p.k;
+        const uint4* src = reinterpret_cast<const uint4*>(p.x + (size_t)t * H * esz);
+        uint4* dst = reinterpret_cast<uint4*>(xs + (size_t)s * H * esz);
+        for (int c0 = lane; c0 < nvec; c0 += 32 * 16) {     // 16 independent loads in flight per lane
+          uint4 v[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            if (c0 + 32 * i < nvec) v[i] = __ldg(src + c0 + 32 * i);
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            if (c0 + 32 * i < nvec) dst[c0 + 32 * i] = v[i];
+        }
+        if (!V::kBf16) {
+          const uint32_t* ssf = reinterpret_cast<const uint32_t*>(p.x_sf + (size_t)t * (H / 32));
+          uint32_t* dsf = reinterpret_cast<uint32_t*>(xs_sf + (size_t)s * (H / 32));
+          for (int c = lane; c < nsf; c += 32) dsf[c] = __ldg(ssf + c);
+        }
       }
       fence_proxy_async_global();
       __threadfence();
       __syncwarp();
-      if (lane == 0) red_release_add(&arrival[e], 1u);
+      if (lane == 0) {
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u)
+          if (es[u] >= 0) red_release_add(&arrival[es[u]], 1u);
+      }
     }
   }
 

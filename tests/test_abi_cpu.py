@@ -123,6 +123,10 @@ def test_workspace_regions_are_disjoint_and_aligned(lib):
         assert off % 256 == 0 and off >= end
         end = off + nb
     assert end <= total
+    # routing chunk table: [E][C] counts and C bad-index words; one chunk up to 2048 assignments
+    assert mm.mm_workspace_region("route_chunks", *shape)[1] == 4 * 16 * 1 + 4
+    assert mm.mm_workspace_region("route_chunks", 20000, 256, 8, 512, 256)[1] == 4 * 256 * 128 + 4 * 128
+    assert mm.mm_workspace_region("route_chunks", 300, 256, 8, 512, 256)[1] == 4 * 256 * 3 + 4 * 3
 
 
 # ---------------------------------------------------------------- argument errors

@@ -41,7 +41,8 @@ def test_routing_of_the_configs(name):
 
 
 @pytest.mark.parametrize("T,E,k,empty", [(1, 1, 1, 0.0), (8, 4, 3, 0.0), (48, 16, 2, 0.3), (192, 1024, 16, 0.1),
-                                         (33, 7, 5, 0.0), (1000, 3, 1, 0.5), (5, 1024, 1, 0.0)])
+                                         (33, 7, 5, 0.0), (1000, 3, 1, 0.5), (5, 1024, 1, 0.0),
+                                         (3001, 37, 7, 0.05), (20000, 256, 8, 0.02)])
 def test_routing_edge_shapes(T, E, k, empty):
     rng = np.random.default_rng(T + E + k)
     idx = rng.integers(0, E, (T, k)).astype(np.int32)          # duplicate experts per token allowed
@@ -60,3 +61,15 @@ def test_bad_index_is_reported():
     st, *_ = _gpu_route(idx, 8)
     assert st[0] == mm.MM_ERR_BAD_INDEX
     assert st[2] == 7 * 2 + 1   # first bad flat index
+
+
+def test_bad_index_is_reported_across_chunks():
+    """Above 2048 assignments the flat array is split into chunks of ~1024;
+    the smallest bad flat index over all chunks is reported."""
+    idx = np.zeros((1000, 8), np.int32)          # 8000 assignments: 8 chunks
+    idx[900, 3] = 16                             # chunk 7
+    idx[400, 5] = -7                             # chunk 3: the first bad one
+    idx[700, 0] = 99
+    st, *_ = _gpu_route(idx, 16)
+    assert st[0] == mm.MM_ERR_BAD_INDEX
+    assert st[2] == 400 * 8 + 5
