@@ -62,7 +62,7 @@ int check_shape(long long T, int E, int k, int H, int I) {
 struct DevState {
   bool ready = false;
   int sms = 0;
-  int max_resident[kNumVariants] = {0, 0};   // layer kernel CTAs resident at once, per variant
+  int max_resident[kNumVariants] = {};   // layer kernel CTAs resident at once, per variant
 };
 
 // Kernel variant for a batch: with at most 16 assignments per expert on
