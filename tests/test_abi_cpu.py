@@ -129,6 +129,14 @@ def test_workspace_regions_are_disjoint_and_aligned(lib):
     assert mm.mm_workspace_region("route_chunks", 300, 256, 8, 512, 256)[1] == 4 * 256 * 3 + 4 * 3
 
 
+@pytest.mark.parametrize("A,chunks", [(1, 1), (2048, 1), (2049, 3), (4096, 4), (4097, 5), (131072, 128),
+                                      (131073, 128), (1 << 24, 128)])
+def test_routing_chunk_count(lib, A, chunks):
+    """One routing CTA up to 2048 assignments, else ceil(A / 1024) chunks, at most 128."""
+    E = 16
+    assert mm.mm_workspace_region("route_chunks", A, E, 1, 128, 128)[1] == 4 * E * chunks + 4 * chunks
+
+
 # ---------------------------------------------------------------- argument errors
 FAKE = 1 << 20        # an aligned address that is never dereferenced
 
