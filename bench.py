@@ -86,19 +86,88 @@ def _profiled_traffic(workload):
     return None
 
 
+class _Nvml:
+    """Read-only NVML queries through ctypes (SM clock and clock-event
+    reasons); ``ok`` is False where the library or the device cannot be opened."""
+
+    SM_CLOCK = 1
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, uuid=None, index=0):
+        import ctypes
+
+        self.ok = False
+        try:
+            self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.lib.nvmlInit_v2() != 0:
+                return
+            self.h = ctypes.c_void_p()
+            rc = 1
+            if uuid:
+                rc = self.lib.nvmlDeviceGetHandleByUUID(("GPU-" + str(uuid)).encode(), ctypes.byref(self.h))
+            if rc != 0:
+                rc = self.lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(self.h))
+            self.ok = rc == 0
+            self.mx = self.clock(max_clock=True)
+        except Exception:
+            self.ok = False
+
+    def clock(self, max_clock=False):
+        import ctypes
+
+        v = ctypes.c_uint(0)
+        fn = self.lib.nvmlDeviceGetMaxClockInfo if max_clock else self.lib.nvmlDeviceGetClockInfo
+        return v.value if fn(self.h, self.SM_CLOCK, ctypes.byref(v)) == 0 else None
+
+    def reasons(self):
+        import ctypes
+
+        v = ctypes.c_ulonglong(0)
+        fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        if fn(self.h, ctypes.byref(v)) != 0:
+            return None
+        return [nm for bit, nm in self.REASONS.items() if v.value & bit]
+
+
 class ClockSampler:
-    """nvidia-smi clock / throttle sampling during the timed region."""
+    """SM clock and throttle reasons sampled DURING the timed region: an NVML
+    thread every millisecond (so that even a region of a few tens of
+    milliseconds gets tens of samples), else nvidia-smi every 100 ms."""
 
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index):
-        self.index = index
+    def __init__(self, index, uuid=None, period_s=0.001):
+        self.index, self.uuid, self.period = index, uuid, period_s
         self.proc = None
+        self.thread = None
+        self.samples = []        # (sm_mhz, [reasons])
+        self.max_mhz = None
+        self.source = None
 
     def __enter__(self):
+        import threading
+
+        nv = _Nvml(self.uuid, self.index)
+        if nv.ok and nv.clock() is not None:
+            self.source, self.max_mhz = "nvml", nv.mx
+            self._stop = threading.Event()
+
+            def run():
+                while not self._stop.is_set():
+                    c, r = nv.clock(), nv.reasons()
+                    if c is not None:
+                        self.samples.append((float(c), r or []))
+                    self._stop.wait(self.period)
+
+            self.thread = threading.Thread(target=run, daemon=True)
+            self.thread.start()
+            return self
         try:
+            self.source = "nvidia-smi"
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
                  "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
@@ -107,7 +176,9 @@ class ClockSampler:
         return self
 
     def __exit__(self, *exc):
-        self.lines = []
+        if self.thread is not None:
+            self._stop.set()
+            self.thread.join(timeout=5)
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -115,28 +186,25 @@ class ClockSampler:
             except Exception:
                 self.proc.kill()
                 out, _ = self.proc.communicate()
-            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            for ln in out.splitlines():
+                f = [x.strip() for x in ln.split(",")]
+                if len(f) < 9:
+                    continue
+                try:
+                    c, self.max_mhz = float(f[1]), float(f[2])
+                except ValueError:
+                    continue
+                self.samples.append((c, [nm for nm, v in zip(names, f[5:9]) if v.lower() == "active"]))
         return False
 
     def summary(self):
-        sm, mx, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in getattr(self, "lines", []):
-            f = [x.strip() for x in ln.split(",")]
-            if len(f) < 9:
-                continue
-            try:
-                sm.append(float(f[1]))
-                mx = float(f[2])
-            except ValueError:
-                continue
-            for nm, v in zip(names, f[5:9]):
-                if v.lower() == "active":
-                    reasons.add(nm)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0, "source": self.source}
+        sm = [c for c, _ in self.samples]
+        reasons = sorted({r for _, rs in self.samples for r in rs})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": self.max_mhz, "sm_min_mhz": min(sm),
+                "reasons": reasons, "samples": len(sm), "source": self.source}
 
 
 def replica_throughput(ms_local, tokens_per_rank, world, max_over_ranks):
@@ -149,32 +217,22 @@ def replica_throughput(ms_local, tokens_per_rank, world, max_over_ranks):
 
 
 # ------------------------------------------------------------------ our arm
-def run_ours(args, rank, world, local_rank):
-    import numpy as np
-    import torch
+PER_CONFIG = ("prefill", "skew", "kimi")       # timed after the headline in the same run (1 GPU)
 
-    import moe_expert_layer_idx_gb300 as mm
-    import synth
 
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
-    mm.lib()                                           # fails loudly if the library is missing
-    cfg = synth.CONFIGS[args.workload]
-    seed = cfg.seed + rank                             # replicas: distinct tokens per rank
-    T, H, I, E, k = cfg.T, cfg.H, cfg.I, cfg.E, cfg.k
+def _quant(mm, src, rows, cols, fmt, out, out_sf):
+    rc = mm.mm_quantize_mx(src, rows, cols, fmt, out, out_sf)
+    if rc != mm.MM_OK:
+        raise RuntimeError(f"mm_quantize_mx: {mm.STATUS_NAMES.get(rc, rc)}")
 
-    # ---- inputs (synthetic, generated and quantised on the device)
-    def quant(src, rows, cols, fmt, out, out_sf):
-        rc = mm.mm_quantize_mx(src, rows, cols, fmt, out, out_sf)
-        if rc != mm.MM_OK:
-            raise RuntimeError(f"mm_quantize_mx: {mm.STATUS_NAMES.get(rc, rc)}")
 
-    bf16_layer = args.layer == "bf16"
+def _make_weights(mm, synth, torch, cfg, dev, bf16_layer):
+    """Seeded expert weights, quantised on the device by the library's own kernel."""
+    E, H, I = cfg.E, cfg.H, cfg.I
     if bf16_layer:
-        # the bf16 x bf16 layer: the same seeded values, rounded to bf16
         l1_w = torch.empty(E, 2 * I, H, dtype=torch.bfloat16, device=dev)
         l2_w = torch.empty(E, H, I, dtype=torch.bfloat16, device=dev)
-        l1_sf = l2_sf = x_sf = None
+        l1_sf = l2_sf = None
     else:
         l1_w = torch.empty(E, 2 * I, H // 2, dtype=torch.uint8, device=dev)
         l1_sf = torch.empty(E, 2 * I, H // 32, dtype=torch.uint8, device=dev)
@@ -189,25 +247,94 @@ def run_ours(args, rank, world, local_rank):
         if bf16_layer:
             l1_w[e0:e1].copy_(buf[:n1].view(e1 - e0, 2 * I, H))
         else:
-            quant(buf[:n1], (e1 - e0) * 2 * I, H, mm.MM_FMT_E2M1, l1_w[e0:e1], l1_sf[e0:e1])
+            _quant(mm, buf[:n1], (e1 - e0) * 2 * I, H, mm.MM_FMT_E2M1, l1_w[e0:e1], l1_sf[e0:e1])
         synth.normal_f32_cuda(cfg.seed, synth.TENSOR_W2, e0 * H * I, buf[:n2], synth.weight_scale(I))
         if bf16_layer:
             l2_w[e0:e1].copy_(buf[:n2].view(e1 - e0, H, I))
         else:
-            quant(buf[:n2], (e1 - e0) * H, I, mm.MM_FMT_E2M1, l2_w[e0:e1], l2_sf[e0:e1])
+            _quant(mm, buf[:n2], (e1 - e0) * H, I, mm.MM_FMT_E2M1, l2_w[e0:e1], l2_sf[e0:e1])
     del buf
+    return l1_w, l1_sf, l2_w, l2_sf
+
+
+def _make_tokens(mm, synth, torch, cfg, seed, dev, bf16_layer):
+    T, H = cfg.T, cfg.H
     xf = torch.empty(T * H, dtype=torch.float32, device=dev)
     synth.normal_f32_cuda(seed, synth.TENSOR_X, 0, xf)
     if bf16_layer:
-        x = xf.view(T, H).to(torch.bfloat16)
+        x, x_sf = xf.view(T, H).to(torch.bfloat16), None
     else:
         x = torch.empty(T, H, dtype=torch.uint8, device=dev)
         x_sf = torch.empty(T, H // 32, dtype=torch.uint8, device=dev)
-        quant(xf, T, H, mm.MM_FMT_E4M3, x, x_sf)
+        _quant(mm, xf, T, H, mm.MM_FMT_E4M3, x, x_sf)
     del xf
     idx_np, w_np, _ = synth.routing(cfg, seed)
-    topk_idx = torch.from_numpy(idx_np).to(dev)
-    topk_w = torch.from_numpy(w_np).to(dev)
+    return x, x_sf, torch.from_numpy(idx_np).to(dev), torch.from_numpy(w_np).to(dev), idx_np
+
+
+def _roofline(cfg, ms, idx_np, bf16_layer, workload, kernel, route_ms=None):
+    """Roofline of one whole step (routing, layer kernel, combine): algorithmic
+    bytes (touched experts' weights + scales, x, x_sf, top-k, y) or FLOPs over
+    the step time, against the measured peak of the bound that is slower."""
+    import numpy as np
+
+    T, H, I, E, k = cfg.T, cfg.H, cfg.I, cfg.E, cfg.k
+    counts = np.bincount(idx_np.reshape(-1)[idx_np.reshape(-1) >= 0], minlength=E)
+    touched = int((counts > 0).sum())
+    if bf16_layer:      # bf16 weights (no scales), bf16 x
+        alg_bytes = touched * (3 * H * I * 2) + T * H * 2 + T * k * 8 + T * H * 2
+    else:
+        alg_bytes = touched * cfg.expert_bytes() + T * H + T * H // 32 + T * k * 8 + T * H * 2
+    hbm, bf16, peak_src = _peaks()
+    achieved_gbs = alg_bytes / (ms * 1e-3) / 1e9
+    achieved_tflops = cfg.flops() / (ms * 1e-3) / 1e12
+    # E4M3 x E2M1 block-scaled MMAs run at the FP8 rate: the measured bf16 peak x the nominal 2
+    mx_tflops = bf16 if bf16_layer else FP8_PER_BF16 * bf16
+    tensor_bound = cfg.flops() / alg_bytes > (mx_tflops * 1e12) / (hbm * 1e9)
+    common = {"peak_source": (f"{peak_src}: MEASURED_PEAKS.json " +
+                              (("bf16_tflops" if bf16_layer else "bf16_tflops x 2 (nominal FP8 / bf16)")
+                               if tensor_bound else "hbm_gbs"))
+              if peak_src == "measured" else "fallback (6.8 TB/s, 1.9 PFLOP/s bf16 x 2)",
+              "kernel": kernel, "time_ms": round(ms, 4),
+              "algorithmic_bytes_per_launch": alg_bytes, "flops_per_launch": cfg.flops(),
+              "touched_experts": touched, "achieved_gbs": round(achieved_gbs, 1),
+              "achieved_tflops": round(achieved_tflops, 1),
+              "hbm_frac": round(achieved_gbs / hbm, 4), "tensor_frac": round(achieved_tflops / mx_tflops, 4)}
+    if route_ms is not None:
+        common["route_ms"] = round(route_ms, 4)
+    if tensor_bound:
+        return {"bound": "tensor", "achieved": round(achieved_tflops, 1), "peak": round(mx_tflops, 1),
+                "unit": "TFLOP/s", "frac": round(achieved_tflops / mx_tflops, 4), "traffic": None, **common}
+    return {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": hbm, "unit": "GB/s",
+            "frac": round(achieved_gbs / hbm, 4), "traffic": _profiled_traffic(workload), **common}
+
+
+def _device_uuid(torch, dev):
+    try:
+        return str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        return None
+
+
+def run_ours(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+
+    import moe_expert_layer_idx_gb300 as mm
+    import synth
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    uuid = _device_uuid(torch, dev)
+    mm.lib()                                           # fails loudly if the library is missing
+    cfg = synth.CONFIGS[args.workload]
+    seed = cfg.seed + rank                             # replicas: distinct tokens per rank
+    T, H, I, E, k = cfg.T, cfg.H, cfg.I, cfg.E, cfg.k
+    bf16_layer = args.layer == "bf16"
+
+    # ---- inputs (synthetic, generated and quantised on the device)
+    l1_w, l1_sf, l2_w, l2_sf = _make_weights(mm, synth, torch, cfg, dev, bf16_layer)
+    x, x_sf, topk_idx, topk_w, idx_np = _make_tokens(mm, synth, torch, cfg, seed, dev, bf16_layer)
     y = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
     ws_bytes = (mm.mm_bf16_workspace_size if bf16_layer else mm.mm_workspace_size)(T, E, k, H, I)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
@@ -224,8 +351,8 @@ def run_ours(args, rank, world, local_rank):
         if rc != mm.MM_OK:
             raise RuntimeError(f"mm_forward: {mm.STATUS_NAMES.get(rc, rc)}")
 
-    def check_status():
-        st, sm, info = mm.mm_get_status(ws, stream)
+    def check_status(w=None):
+        st, sm, info = mm.mm_get_status(ws if w is None else w, stream)
         if st != mm.MM_OK:
             raise RuntimeError(f"device status {mm.STATUS_NAMES.get(st, st)} sm={sm} info={info:#x}")
 
@@ -246,7 +373,7 @@ def run_ours(args, rank, world, local_rank):
     # ---- timed region: K whole-layer steps, inputs resident
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
-    with ClockSampler(local_rank) as clk:
+    with ClockSampler(local_rank, uuid) as clk:
         t_wall = time.perf_counter()
         ev0.record(stream)
         for _ in range(args.steps):
@@ -276,7 +403,7 @@ def run_ours(args, rank, world, local_rank):
            "p90": round(float(np.percentile(per_step, 90)), 4), "steps": n_pct}
     check_status()
 
-    # ---- routing kernel alone (to isolate the time of the layer kernel and its combine kernel)
+    # ---- routing kernel(s) alone: reported beside the whole-step roofline
     ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ea.record(stream)
     for _ in range(args.steps):
@@ -285,7 +412,6 @@ def run_ours(args, rank, world, local_rank):
     eb.record(stream)
     eb.synchronize()
     route_ms = ea.elapsed_time(eb) / args.steps
-    kernel_ms = max(ms - route_ms, 1e-6)
 
     # ---- end to end through the C ABI: pinned host inputs -> device -> layer -> host
     hx = x.cpu().pin_memory()
@@ -318,48 +444,91 @@ def run_ours(args, rank, world, local_rank):
     h2d = hx.numel() * hx.element_size() + (hsf.numel() if hsf is not None else 0) + hidx.numel() * 4 + hw.numel() * 4
     d2h = hy.numel() * 2
 
-    # ---- roofline of the layer kernel (HBM-bound at the decode batch)
-    counts = np.bincount(idx_np.reshape(-1)[idx_np.reshape(-1) >= 0], minlength=E)
-    touched = int((counts > 0).sum())
-    if bf16_layer:      # bf16 weights (no scales), bf16 x
-        alg_bytes = touched * (3 * H * I * 2) + T * H * 2 + T * k * 8 + T * H * 2
-    else:
-        alg_bytes = (touched * cfg.expert_bytes() + T * H + T * H // 32 + T * k * 8 + T * H * 2)
-    hbm, bf16, peak_src = _peaks()
-    achieved_gbs = alg_bytes / (kernel_ms * 1e-3) / 1e9
-    achieved_tflops = cfg.flops() / (kernel_ms * 1e-3) / 1e12
-    # E4M3 x E2M1 block-scaled MMAs run at the FP8 rate: the measured bf16 peak x the nominal 2
-    mx_tflops = bf16 if bf16_layer else FP8_PER_BF16 * bf16
-    tensor_bound = cfg.flops() / alg_bytes > (mx_tflops * 1e12) / (hbm * 1e9)
-    common = {"peak_source": (f"{peak_src}: MEASURED_PEAKS.json " +
-                              (("bf16_tflops" if bf16_layer else "bf16_tflops x 2 (nominal FP8 / bf16)")
-                               if tensor_bound else "hbm_gbs"))
-              if peak_src == "measured" else "fallback (6.8 TB/s, 1.9 PFLOP/s bf16 x 2)",
-              "kernel": "megamoe_kernel + combine_kernel", "kernel_ms": round(kernel_ms, 4),
-              "algorithmic_bytes_per_launch": alg_bytes, "flops_per_launch": cfg.flops(),
-              "touched_experts": touched, "achieved_gbs": round(achieved_gbs, 1),
-              "achieved_tflops": round(achieved_tflops, 1)}
-    if tensor_bound:
-        roofline = {"bound": "tensor", "achieved": round(achieved_tflops, 1), "peak": round(mx_tflops, 1),
-                    "unit": "TFLOP/s", "frac": round(achieved_tflops / mx_tflops, 4), "traffic": None, **common}
-    else:
-        roofline = {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": hbm, "unit": "GB/s",
-                    "frac": round(achieved_gbs / hbm, 4), "traffic": _profiled_traffic(args.workload), **common}
+    roofline = _roofline(cfg, ms, idx_np, bf16_layer, args.workload,
+                         "whole step: routing + megamoe_kernel + combine_kernel", route_ms)
+    launches_per_step = (1 if T * k <= 2048 else 3) + 2
+
+    # ---- the other full-size configurations, timed the same way (1 GPU only)
+    per_config = {}
+    if world == 1 and not bf16_layer and args.per_config:
+        del hx, hsf, hidx, hw, hy, ws
+        weights = (l1_w, l1_sf, l2_w, l2_sf)
+        for name in args.per_config:
+            pc = synth.CONFIGS[name]
+            if (pc.E, pc.H, pc.I) != (E, H, I):
+                weights = None
+                del l1_w, l1_sf, l2_w, l2_sf
+                torch.cuda.empty_cache()
+                l1_w, l1_sf, l2_w, l2_sf = _make_weights(mm, synth, torch, pc, dev, False)
+                weights = (l1_w, l1_sf, l2_w, l2_sf)
+                E, H, I = pc.E, pc.H, pc.I
+            per_config[name] = _time_config(mm, synth, torch, np, pc, weights, dev, stream, uuid, local_rank,
+                                            args.per_config_steps, max(3, args.warmup))
+            launches_per_step_pc = (1 if pc.T * pc.k <= 2048 else 3) + 2
+            per_config[name]["gpu_launches"] = launches_per_step_pc * per_config[name]["steps"]
     return {
         "tokens_per_s": tokens_per_s, "ms": ms, "route_ms": route_ms, "roofline": roofline,
         "e2e": {"value": round(e2e_tps, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
-        "clocks": clk.summary(), "wall_s": t_wall, "gpu_launches": ((1 if T * k <= 2048 else 3) + 2) * args.steps, "step_ms": pct,
-        "cfg": cfg, "touched": touched,
+        "clocks": clk.summary(), "wall_s": t_wall, "gpu_launches": launches_per_step * args.steps, "step_ms": pct,
+        "cfg": cfg, "per_config": per_config,
     }
 
 
-# ------------------------------------------------------------------ oracle
-def run_oracle_sample(workload, sample_tokens, time_budget_s=25.0, layer="fp8"):
-    """Time the CPU oracle (fp64, plain numpy) on the first tokens of the same
-    workload.  Returns (tokens/s, threads, sample description)."""
-    import numpy as np
+def _time_config(mm, synth, torch, np, cfg, weights, dev, stream, uuid, local_rank, steps, warmup):
+    """One full-size configuration: W warm-up steps, then K steps between CUDA
+    events on the launching stream with the clocks sampled meanwhile; the
+    roofline of the whole step.  The expert weights are resident (several GB,
+    far beyond L2), so no flush is needed."""
+    T, H, I, E, k = cfg.T, cfg.H, cfg.I, cfg.E, cfg.k
+    l1_w, l1_sf, l2_w, l2_sf = weights
+    x, x_sf, topk_idx, topk_w, idx_np = _make_tokens(mm, synth, torch, cfg, cfg.seed, dev, False)
+    y = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    ws_bytes = mm.mm_workspace_size(T, E, k, H, I)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
 
+    def step():
+        rc = mm.mm_forward(T, E, k, H, I, x, x_sf, topk_idx, topk_w, l1_w, l1_sf, l2_w, l2_sf, y, cfg.clamp, 0,
+                           ws, ws_bytes, stream)
+        if rc != mm.MM_OK:
+            raise RuntimeError(f"mm_forward ({cfg.name}): {mm.STATUS_NAMES.get(rc, rc)}")
+
+    for _ in range(warmup):
+        step()
+    st, sm, info = mm.mm_get_status(ws, stream)
+    if st != mm.MM_OK:
+        raise RuntimeError(f"{cfg.name}: device status {mm.STATUS_NAMES.get(st, st)} sm={sm} info={info:#x}")
+    torch.cuda.synchronize(dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank, uuid) as clk:
+        ev0.record(stream)
+        for _ in range(steps):
+            step()
+        ev1.record(stream)
+        ev1.synchronize()
+    st, sm, info = mm.mm_get_status(ws, stream)
+    if st != mm.MM_OK:
+        raise RuntimeError(f"{cfg.name}: device status {mm.STATUS_NAMES.get(st, st)} sm={sm} info={info:#x}")
+    ms = ev0.elapsed_time(ev1) / steps
+    out = {"workload": f"{cfg.name}: {T} tokens, hidden {H}, inter {I}, {E} experts, top-{k}, "
+                       f"E4M3 x E2M1 with UE8M0/32, clamp {cfg.clamp if cfg.clamp else 'none'}",
+           "steps": steps, "warmup": warmup, "ms_per_step": round(ms, 4), "tokens_per_s": round(T / (ms * 1e-3), 1),
+           "roofline": _roofline(cfg, ms, idx_np, False, cfg.name,
+                                 "whole step: routing + megamoe_kernel + combine_kernel"),
+           "clocks": clk.summary()}
+    if cfg.name == "kimi":
+        out["note"] = ("default reserve of 2 SMs, no side stream; the side-stream and graph-replay runs of this "
+                       "configuration are parity tests")
+    del x, x_sf, topk_idx, topk_w, y, ws
+    return out
+
+
+# ------------------------------------------------------------------ oracle
+def _oracle_sample(workload, sample_tokens, layer="fp8"):
+    """Prepare a bounded sample of the workload for the CPU oracle (fp64, plain
+    numpy): the first `sample_tokens` tokens and the experts they touch (expert
+    weights quantised by the oracle).  Returns (run, description, threads)
+    where run() is one oracle forward over the sample."""
     import synth
     from oracle import formats as OF
     from oracle import moe as OM
@@ -367,27 +536,55 @@ def run_oracle_sample(workload, sample_tokens, time_budget_s=25.0, layer="fp8"):
 
     cfg = synth.CONFIGS[workload]
     idx, w, _ = synth.routing(cfg)
-    n = max(1, sample_tokens)
-    toks = list(range(min(n, cfg.T)))
+    toks = list(range(min(max(1, sample_tokens), cfg.T)))
     experts = sorted({int(e) for e in idx[toks].reshape(-1) if e >= 0})
     tp = time.perf_counter()
     if layer == "bf16":
         xb = OF.bf16_round(synth.x_f32(cfg, rows=toks))
         cache = {e: (OF.bf16_round(synth.w1_f32(cfg, e)), OF.bf16_round(synth.w2_f32(cfg, e))) for e in experts}
+        run = lambda: OMB.moe_forward_bf16(xb, idx[toks], w[toks], lambda e: cache[e], cfg.clamp, cfg.E)  # noqa: E731
     else:
         xc, xsf = OF.quantize_mx(synth.x_f32(cfg, rows=toks), OF.E4M3)
         cache = {e: OM.quantize_expert(synth.w1_f32(cfg, e), synth.w2_f32(cfg, e)) for e in experts}
+        run = lambda: OM.moe_forward(xc, xsf, idx[toks], w[toks], lambda e: cache[e], cfg.clamp, cfg.E)  # noqa: E731
     _log(f"oracle sample: {len(experts)} experts prepared in {time.perf_counter() - tp:.1f} s")
-    t0 = time.perf_counter()
-    if layer == "bf16":
-        OMB.moe_forward_bf16(xb, idx[toks], w[toks], lambda e: cache[e], cfg.clamp, cfg.E)
-    else:
-        OM.moe_forward(xc, xsf, idx[toks], w[toks], lambda e: cache[e], cfg.clamp, cfg.E)
-    dt = time.perf_counter() - t0
     threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
     desc = (f"first {len(toks)} token(s) of the {workload} batch ({len(experts)} experts, "
             f"{len(toks) * cfg.k} assignments); fp64 numpy oracle, BLAS threads default")
-    return len(toks) / dt, threads, desc, dt
+    return run, desc, threads, len(toks)
+
+
+def run_oracle_sample(workload, sample_tokens, layer="fp8"):
+    """Time one oracle forward over the sample.  Returns (tokens/s, threads,
+    sample description, seconds)."""
+    run, desc, threads, n = _oracle_sample(workload, sample_tokens, layer)
+    t0 = time.perf_counter()
+    run()
+    dt = time.perf_counter() - t0
+    return n / dt, threads, desc, dt
+
+
+def run_reference(args, config):
+    """The reference arm: the oracle, as it stands, on the host cores.  Every
+    step is one oracle forward over the same bounded sample of the workload;
+    W untimed warm-up steps, then exactly K timed steps."""
+    run, desc, threads, n = _oracle_sample(args.workload, args.ref_sample_tokens, args.layer)
+    for _ in range(args.warmup):
+        run()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run()
+    dt = time.perf_counter() - t0
+    ms = 1e3 * dt / args.steps
+    tps = n / (ms * 1e-3)
+    return {"impl": "reference", "metric": METRIC, "value": round(tps, 4), "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config,
+            "cpu_baseline": {"value": round(tps, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": f"each step: {desc}", "tokens_per_step": n,
+                             "timed_seconds": round(dt, 2)},
+            "e2e": {"value": round(tps, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
 # ------------------------------------------------------------------ main
@@ -401,11 +598,17 @@ def main():
     ap.add_argument("--layer", choices=["fp8", "bf16"], default="fp8",
                     help="fp8: E4M3 x E2M1 (the default); bf16: the bf16 x bf16 layer")
     ap.add_argument("--cpu-sample-tokens", type=int, default=8)
+    ap.add_argument("--ref-sample-tokens", type=int, default=1,
+                    help="tokens per step of the reference arm (the oracle)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--per-config", default=",".join(PER_CONFIG),
+                    help="full-size configurations timed after the headline (1 GPU); empty for none")
+    ap.add_argument("--per-config-steps", type=int, default=20)
     ap.add_argument("--tokens", type=int, default=0, help="override the token count (profiling of small cases)")
     ap.add_argument("--experts", type=int, default=0, help="override the expert count (profiling of small cases)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    args.per_config = [c for c in args.per_config.split(",") if c and c != args.workload]
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -421,6 +624,7 @@ def main():
                                   T=args.tokens or cfg.T, E=args.experts or cfg.E)
         synth.CONFIGS[cfg.name] = cfg
         args.workload = cfg.name
+        args.per_config = []
     config = {"workload": f"{cfg.name}: {cfg.T} tokens, hidden {cfg.H}, inter {cfg.I}, {cfg.E} experts, "
                           f"top-{cfg.k}, "
                           f"{'bf16 x bf16' if args.layer == 'bf16' else 'E4M3 x E2M1 with UE8M0/32'}, "
@@ -432,15 +636,7 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return 0
-        tps, threads, desc, dt = run_oracle_sample(args.workload, args.cpu_sample_tokens, layer=args.layer)
-        line = {"impl": "reference", "metric": METRIC, "value": round(tps, 4), "unit": UNIT, "n_gpus": args.gpus,
-                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * cfg.T / tps, 3),
-                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-                "data": "synthetic", "config": config,
-                "cpu_baseline": {"value": round(tps, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
-                                 "sample": desc},
-                "e2e": {"value": round(tps, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-        print(json.dumps(line), flush=True)
+        print(json.dumps(run_reference(args, config)), flush=True)
         return 0
 
     if world > 1:
@@ -473,6 +669,8 @@ def main():
             "data": "synthetic", "config": config, "roofline": res["roofline"], "cpu_baseline": cpu,
             "e2e": res["e2e"], "gpu_launches": res["gpu_launches"], "clocks": res["clocks"],
             "route_ms": round(res["route_ms"], 4), "step_ms_percentiles": res["step_ms"]}
+    if res["per_config"]:
+        line["per_config"] = res["per_config"]
     print(json.dumps(line), flush=True)
     return 0
 

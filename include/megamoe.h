@@ -19,9 +19,10 @@
  *       and a symmetric-buffer cache keyed only on the shape.
  *  [P3] DeepGEMM "SM90 MegaMoE 开发日志" -- Phase 1 entry (the buffer views
  *       x, x_sf, topk_idx, topk_weights, l1_acts, l1_acts_sf, l2_acts,
- *       l2_acts_sf; a workspace-size query) and Phase 2 entry (dispatch:
- *       workspace clean, expert count, source token-topk index write,
- *       token source metadata, l1_arrival_count release).
+ *       l2_acts_sf; a workspace-size query) and Phase 2 entry (the dispatch
+ *       clears its workspace, counts each expert's assignments, records the
+ *       source (token, k) of every slot and releases a per-expert arrival
+ *       count once the expert's rows are in place).
  *  [P4] DeepGEMM PR #451 "[Bugfix] Reset MegaMoE combine readiness for CUDA
  *       graph replay": readiness flags are reset by every launch, never keyed
  *       on %gridid, so graph replays match eager runs exactly.
@@ -82,8 +83,8 @@ typedef enum { MM_FMT_E4M3 = 0, MM_FMT_E2M1 = 1 } mm_format;
  * need for up to `max_tokens` tokens.  Depends only on the shape, never on the
  * SM count or the reserve (the cache key of [P2] 实现拆解 item 5 holds only
  * shape parameters).  Returns 0 for unsupported arguments.
- * Workspace contents: a control block (status, abort flag, grid-barrier and
- * readiness counters), routing results (counts, offsets, permutation), the
+ * Workspace contents: a control block (status, abort flag, tile counter),
+ * per-expert readiness counters, routing results (counts, offsets, permutation), the
  * dispatched tokens and their scales in expert order, the L1 activations
  * (E4M3 + UE8M0/32) and the weighted L2 outputs (fp32) -- the views of [P3].
  */
@@ -117,7 +118,8 @@ size_t mm_workspace_size(int max_tokens, int experts, int topk, int hidden, int 
  *   stream    the stream to enqueue on.
  *
  * Enqueues the routing (one kernel, or three above 2048 assignments), the
- * persistent layer kernel, then the top-k combine, and returns.  T = 0 returns MM_OK without launching.  Device-side errors land in
+ * persistent layer kernel, then the top-k combine, and returns.  T = 0
+ * returns MM_OK without launching.  Device-side errors land in
  * the workspace status (mm_get_status); the next mm_forward resets it.  Every
  * device wait is bounded by mm_set_wait_timeout_ns; a wait that runs out sets
  * MM_ERR_TIMEOUT and the kernel returns instead of hanging.  The call makes
@@ -277,31 +279,45 @@ int mm_quantize_mx(const float* src, long long rows, long long cols, int fmt,
  * pages have no counterpart to this entry point.
  *
  * Some callers cannot allocate device memory at the point where they run the
- * layer: code running while a stream is being captured into a CUDA graph
- * (cudaMalloc is not permitted during capture), inference runtimes whose
- * device memory is entirely owned by their own pool allocator, and real-time
- * loops that forbid allocation after start-up.  For them the library keeps
- * one fixed scratch array of 48 MiB in device memory (a file-scope __device__
- * array, present on every GPU where the library's kernels are loaded until
- * the process exits), enough for a decode batch of the DeepSeek-sized layer
- * (128 tokens, top-8, hidden 7168, inter 2048 needs 39 MB).
+ * layer: inference runtimes whose device memory is entirely owned by their
+ * own pool allocator (a cudaMalloc behind its back fails or breaks its
+ * accounting), plugins that run inside such a host and are handed only their
+ * inputs and outputs, and real-time or safety-certified loops that forbid any
+ * allocation after start-up.  For them the library keeps one fixed scratch
+ * array of 48 MiB in device memory (a file-scope __device__ array, present on
+ * every GPU where the library's kernels are loaded until the process exits),
+ * enough for a decode batch of the DeepSeek-sized layer (128 tokens, top-8,
+ * hidden 7168, inter 2048 needs 39 MB).
  *
  * Arguments are those of mm_forward minus the workspace.  A shape whose
  * workspace (mm_workspace_size) exceeds 48 MiB is rejected with
  * MM_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.  No cudaMalloc,
  * cudaFree or allocating routine is called.  The first call on a device looks
  * up the array's device address (cudaGetSymbolAddress, with that device
- * current); make that first call before any stream capture.  Every call on a
- * device shares the same array, and each launch resets what must start at
- * zero; two calls whose kernels overlap on the GPU (different streams, or
- * different host threads) race on it.  Device-side errors are recorded in the
- * array's status word, which mm_get_status cannot reach: after such an error
- * the output is undefined, and the next call resets the status.
+ * current); make that first call before any stream capture begins.  Every
+ * call on a device shares the same array, and each launch resets what must
+ * start at zero; two calls whose kernels overlap on the GPU (different
+ * streams, or different host threads) race on it.  Device-side errors are
+ * recorded in the array's status word: read them with mm_noalloc_get_status;
+ * after such an error the output is undefined, and the next call resets the
+ * status.
  */
 int mm_forward_noalloc(int num_tokens, int experts, int topk, int hidden, int inter,
                        const void* x, const void* x_sf, const int32_t* topk_idx, const float* topk_w,
                        const void* l1_w, const void* l1_sf, const void* l2_w, const void* l2_sf,
                        void* y, float clamp, int num_sms, mm_stream_t stream);
+
+/*
+ * mm_noalloc_get_status -- mm_get_status for the calls of
+ * mm_forward_noalloc on the current device: synchronises `stream`, then reads
+ * the status word at the head of the library's scratch array.  *sm and *info
+ * (either may be NULL) as for mm_get_status.  Returns the recorded mm_status
+ * (MM_OK if none, or if mm_forward_noalloc never ran on this device),
+ * MM_ERR_NO_DEVICE without a current device, or MM_ERR_CUDA if the address
+ * lookup, the synchronisation or the copy failed.  No counterpart on the
+ * pages; it allocates nothing.
+ */
+int mm_noalloc_get_status(mm_stream_t stream, int* sm, int* info);
 
 #ifdef __cplusplus
 }

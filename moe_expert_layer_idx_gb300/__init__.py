@@ -50,6 +50,7 @@ _SIGS = {
     "mm_workspace_region": (_c_int, [_c_int] * 6 + [_c_vp, _c_vp]),
     "mm_quantize_mx": (_c_int, [_c_vp, _c_ll, _c_ll, _c_int, _c_vp, _c_vp, _c_vp]),
     "mm_forward_noalloc": (_c_int, [_c_int] * 5 + [_c_vp] * 9 + [ctypes.c_float, _c_int, _c_vp]),
+    "mm_noalloc_get_status": (_c_int, [_c_vp, _c_vp, _c_vp]),
     "mm_forward_bf16": (_c_int, [_c_int] * 5 + [_c_vp] * 8 + [ctypes.c_float, _c_int, _c_vp, _c_size, _c_vp]),
     "mm_bf16_workspace_size": (_c_size, [_c_int] * 5),
     "mm_bf16_forward": (_c_int, [_c_int] * 5 + [_c_vp] * 6 + [ctypes.c_float, _c_int, _c_vp, _c_size, _c_vp]),
@@ -200,10 +201,18 @@ def mm_quantize_mx(src, rows, cols, fmt, dst, dst_sf, stream=None) -> int:
 def mm_forward_noalloc(num_tokens, experts, topk, hidden, inter, x, x_sf, topk_idx, topk_w, l1_w, l1_sf,
                        l2_w, l2_sf, y, clamp, num_sms, stream=None) -> int:
     """mm_forward with the library's fixed 48 MiB device scratch as workspace,
-    for callers that cannot allocate device memory (see include/megamoe.h)."""
+    for callers that cannot allocate device memory (see include/megamoe.h);
+    device-side errors are read with mm_noalloc_get_status."""
     return lib().mm_forward_noalloc(num_tokens, experts, topk, hidden, inter, _ptr(x), _ptr(x_sf),
                                     _ptr(topk_idx), _ptr(topk_w), _ptr(l1_w), _ptr(l1_sf), _ptr(l2_w),
                                     _ptr(l2_sf), _ptr(y), float(clamp), num_sms, _stream(stream))
+
+
+def mm_noalloc_get_status(stream=None):
+    """Status of the calls of mm_forward_noalloc on the current device: (status, sm, info)."""
+    sm, info = ctypes.c_int(0), ctypes.c_int(0)
+    rc = lib().mm_noalloc_get_status(_stream(stream), ctypes.addressof(sm), ctypes.addressof(info))
+    return rc, sm.value, info.value
 
 
 # ------------------------------------------------------------------ convenience

@@ -97,16 +97,17 @@ enum VariantId : int {
 
 
 // ----------------------------------------------------------------- control block
-// 32-bit words at the head of the workspace.
+// 32-bit words at the head of the workspace (words 4 and 7..63 are unused).
 enum CtrlWord : int {
-  kStatus = 0, kErrSm = 1, kErrInfo = 2, kAbort = 3, kUnused4 = 4, kSiteMask = 5, kNextTile = 6, kCtrlWords = 64
+  kStatus = 0, kErrSm = 1, kErrInfo = 2, kAbort = 3, kSiteMask = 5, kNextTile = 6, kCtrlWords = 64
 };
 
 
-// Wait sites recorded in the error info word (site << 24 | tile & 0xFFFFFF).
+// Wait sites recorded in the error info word (site << 24 | tile & 0xFFFFFF);
+// the numbers are part of the reported value, so a retired site keeps its gap.
 enum WaitSite : uint32_t {
   kSiteFull = 1, kSiteEmpty = 2, kSiteTmemFull = 3, kSiteTmemEmpty = 4,
-  kSiteArrival = 5, kSiteL1Done = 6, kSiteUnused7 = 7, kSiteDrain = 8, kSiteFullSf = 9, kSiteTileRing = 10
+  kSiteArrival = 5, kSiteL1Done = 6, kSiteDrain = 8, kSiteFullSf = 9, kSiteTileRing = 10
 };
 
 // ----------------------------------------------------------------- workspace
@@ -329,14 +330,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
-
-// ---- cp.async (4-byte) for the scale-factor transposition
-__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" :: "r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
 
 // ---- tcgen05
 __device__ __forceinline__ void tc_alloc(uint32_t dst_smem, uint32_t ncols) {

@@ -1,6 +1,7 @@
 // mm_forward_noalloc: the fused layer with its workspace in a fixed device
 // array that the library owns, for callers that cannot allocate device
-// memory themselves (see include/megamoe.h for who they are and why).
+// memory themselves (see include/megamoe.h for who they are and why), and
+// mm_noalloc_get_status, which reads the status word of that array.
 //
 // The scratch array below is a file-scope __device__ variable: it exists on
 // every GPU where this library's kernels are loaded and stays there until the
@@ -21,6 +22,28 @@ static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes]
 std::mutex g_noalloc_mu;
 void* g_noalloc_ptr[128] = {};   // device address of the array, per device ordinal
 
+// Device address of the array on device `dev` (current), looked up once per
+// device; MM_OK or MM_ERR_CUDA.
+int scratch_address(int dev, void** out) {
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+      cudaGetLastError();
+      return MM_ERR_CUDA;
+    }
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return MM_OK;
+}
+
+int current_device(int* dev) {
+  if (cudaGetDevice(dev) != cudaSuccess) { cudaGetLastError(); return MM_ERR_NO_DEVICE; }
+  if (*dev < 0 || *dev >= 128) return MM_ERR_NO_DEVICE;
+  return MM_OK;
+}
+
 }  // namespace
 
 extern "C" int mm_forward_noalloc(int num_tokens, int experts, int topk, int hidden, int inter,
@@ -37,21 +60,23 @@ extern "C" int mm_forward_noalloc(int num_tokens, int experts, int topk, int hid
   if (num_tokens == 0) return MM_OK;
 
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return MM_ERR_NO_DEVICE; }
-  if (dev < 0 || dev >= 128) return MM_ERR_NO_DEVICE;
+  int rc = current_device(&dev);
+  if (rc != MM_OK) return rc;
   void* ws = nullptr;
-  {
-    std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (!g_noalloc_ptr[dev]) {
-      void* p = nullptr;
-      if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
-        cudaGetLastError();
-        return MM_ERR_CUDA;
-      }
-      g_noalloc_ptr[dev] = p;
-    }
-    ws = g_noalloc_ptr[dev];
-  }
+  rc = scratch_address(dev, &ws);
+  if (rc != MM_OK) return rc;
   return mm_forward(num_tokens, experts, topk, hidden, inter, x, x_sf, topk_idx, topk_w, l1_w, l1_sf, l2_w, l2_sf,
                     y, clamp, num_sms, ws, kNoAllocScratchBytes, stream);
+}
+
+// The status word lives at the head of the array, as at the head of any
+// workspace, so mm_get_status reads it once the array's address is known.
+extern "C" int mm_noalloc_get_status(mm_stream_t stream, int* sm, int* info) {
+  int dev = 0;
+  int rc = current_device(&dev);
+  if (rc != MM_OK) return rc;
+  void* ws = nullptr;
+  rc = scratch_address(dev, &ws);
+  if (rc != MM_OK) return rc;
+  return mm_get_status(ws, stream, sm, info);
 }

@@ -1,9 +1,10 @@
 // Routing: per-launch reset, expert histogram, prefix scan, stable
 // permutation and the per-expert N-block table of the persistent kernel.
 //
-// The pages' kernel does this as its dispatch prologue ("workspace clean ->
-// expert count -> source token-topk index write", DeepGEMM SM90 MegaMoE dev
-// log, Phase 2 entry) and resets its readiness flags on every launch (DeepGEMM
+// The pages' kernel does this as the first part of its dispatch: it clears
+// its workspace, counts the assignments of each expert and records, for every
+// slot, which (token, k) pair it came from (DeepGEMM SM90 MegaMoE dev log,
+// Phase 2 entry); and it resets its readiness flags on every launch (DeepGEMM
 // PR #451, "Reset MegaMoE combine readiness for CUDA graph replay").
 //
 // The flat (t*k + j) array is cut into contiguous pieces, each walked in

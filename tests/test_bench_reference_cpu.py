@@ -16,7 +16,7 @@ def _run(extra_env, *args):
 
 
 def test_reference_arm_prints_one_line_with_the_contract_keys():
-    r = _run({}, "--workload", "tiny", "--steps", "3", "--warmup", "3", "--cpu-sample-tokens", "4")
+    r = _run({}, "--workload", "tiny", "--steps", "3", "--warmup", "3", "--ref-sample-tokens", "4")
     assert r.returncode == 0, r.stderr[-2000:]
     lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
     assert len(lines) == 1
@@ -28,6 +28,10 @@ def test_reference_arm_prints_one_line_with_the_contract_keys():
     assert d["config"]["tokens"] == 64 and d["config"]["experts"] == 8
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and "first 4" in cb["sample"]
+    # the line describes what was timed: K steps of the stated sample
+    assert cb["tokens_per_step"] == 4
+    assert abs(d["steps"] * d["ms_per_step"] / 1e3 - cb["timed_seconds"]) <= 0.02 + 0.01 * cb["timed_seconds"]
+    assert abs(d["value"] - 4 / (d["ms_per_step"] / 1e3)) <= 1e-3 * d["value"] + 1e-3
     assert d["e2e"] == {"value": d["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
 
 

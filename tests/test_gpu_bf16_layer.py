@@ -12,7 +12,7 @@ import torch
 import moe_expert_layer_idx_gb300 as mm
 import synth
 from oracle import moe_bf16 as MB
-from layer_inputs import TOL_MAXREL, TOL_NL2, bf16_to_np
+from layer_inputs import TOL_MAXREL, TOL_NL2, bf16_to_np, close_enough
 
 pytestmark = pytest.mark.gpu
 
@@ -88,12 +88,24 @@ def case(request):
     return cfg, idx, w, y, y2
 
 
-def test_bf16_layer_matches_oracle(case):
+# Cases that also meet the FP8 layer's plain criterion (normalised L2 <= 5e-3
+# and max relative error <= 3e-2 over |ref| > 1e-2, no row floor); the others
+# only report it.
+PLAIN_OK = {"tiny", "thin", "sparse"}     # measured: ragged reaches max rel 0.046 (the row floor covers it)
+
+
+def test_bf16_layer_matches_oracle(case, record_property):
     cfg, idx, w, y, y2 = case
     xo = _host_bf16(synth.x_f32(cfg))
     ref = MB.moe_forward_bf16(xo, idx, w, lambda e: (_host_bf16(synth.w1_f32(cfg, e)), _host_bf16(synth.w2_f32(cfg, e))),
                               cfg.clamp, cfg.E)
-    ok, nl2, excess = close_enough_rows(bf16_to_np(y), ref)
+    got = bf16_to_np(y)
+    plain_ok, plain_nl2, plain_mr = close_enough(got, ref)
+    record_property("plain_criterion", {"ok": plain_ok, "nl2": plain_nl2, "maxrel": plain_mr})
+    print(f"bf16 layer {cfg.name}: plain criterion ok={plain_ok} nl2={plain_nl2:.3g} maxrel={plain_mr:.3g}")
+    if cfg.name in PLAIN_OK:
+        assert plain_ok, (cfg.name, plain_nl2, plain_mr)
+    ok, nl2, excess = close_enough_rows(got, ref)
     assert ok, (cfg.name, nl2, excess)
 
 

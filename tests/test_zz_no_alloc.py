@@ -1,25 +1,28 @@
 """mm_forward_noalloc: the layer for callers that cannot allocate device
-memory (a stream under CUDA-graph capture, a runtime whose pool allocator owns
-all device memory, a loop that forbids allocation after start-up).  Its
-workspace is the library's fixed 48 MiB device array.
+memory where they run it (a runtime whose pool allocator owns all device
+memory, a plugin handed only its inputs and outputs, a loop that forbids
+allocation after start-up).  Its workspace is the library's fixed 48 MiB
+device array, and mm_noalloc_get_status reads that array's status word.
 
 Checked through the C ABI against mm_forward with a caller-owned workspace,
 within the layer's output tolerance, on two calls in a row with different
-inputs; and a shape whose workspace exceeds the array is refused before
-anything is enqueued.  This file is collected last on purpose."""
+inputs; against the oracle on one shape; a shape whose workspace exceeds the
+array is refused before anything is enqueued; and a bad expert index put into
+the input on the host is reported through mm_noalloc_get_status, after which
+a clean call succeeds.  This file is collected last on purpose."""
+import numpy as np
 import pytest
 import torch
 
 import moe_expert_layer_idx_gb300 as mm
 import synth
-from layer_inputs import GpuTokens, GpuWeights, bf16_to_np, close_enough
+from oracle import moe as OM
+from layer_inputs import ExpertCache, GpuTokens, GpuWeights, bf16_to_np, close_enough, oracle_tokens
 
 pytestmark = pytest.mark.gpu
 
-CASES = [
-    synth.CONFIGS["tiny"],
-    synth.Config("noalloc-mid", T=96, H=1024, I=512, E=24, k=4, clamp=7.0, seed=4),
-]
+MID = synth.Config("noalloc-mid", T=96, H=1024, I=512, E=24, k=4, clamp=7.0, seed=4)
+CASES = [synth.CONFIGS["tiny"], MID]
 
 
 def _noalloc(cfg, w, tok):
@@ -27,7 +30,6 @@ def _noalloc(cfg, w, tok):
     rc = mm.mm_forward_noalloc(cfg.T, cfg.E, cfg.k, cfg.H, cfg.I, tok.x, tok.x_sf, tok.topk_idx, tok.topk_w,
                                w.l1_w, w.l1_sf, w.l2_w, w.l2_sf, y, cfg.clamp, 0)
     assert rc == mm.MM_OK, mm.STATUS_NAMES.get(rc, rc)
-    torch.cuda.synchronize()
     return y
 
 
@@ -48,10 +50,41 @@ def test_noalloc_matches_workspace_path_two_calls(cfg):
     for seed in (cfg.seed, cfg.seed + 100):           # two calls in a row, different tokens
         tok = GpuTokens(cfg, seed=seed)
         got = _noalloc(cfg, w, tok)
+        st, sm, info = mm.mm_noalloc_get_status()
+        assert st == mm.MM_OK, (mm.STATUS_NAMES.get(st, st), sm, info)
         want = _with_workspace(cfg, w, tok)
         ok, nl2, mr = close_enough(bf16_to_np(got), bf16_to_np(want))
         assert ok, (cfg.name, seed, nl2, mr)
         assert torch.equal(got.view(torch.int16), want.view(torch.int16))
+
+
+def test_noalloc_matches_oracle():
+    cfg = MID
+    w = GpuWeights(cfg)
+    tok = GpuTokens(cfg)
+    got = _noalloc(cfg, w, tok)
+    assert mm.mm_noalloc_get_status()[0] == mm.MM_OK
+    xc, xsf = oracle_tokens(cfg)
+    ref = OM.moe_forward(xc, xsf, tok.idx_np, tok.w_np, ExpertCache(cfg), cfg.clamp, cfg.E)
+    ok, nl2, mr = close_enough(bf16_to_np(got), ref)
+    assert ok, (nl2, mr)
+
+
+def test_noalloc_reports_a_bad_index_then_recovers():
+    cfg = synth.CONFIGS["tiny"]
+    routing = synth.routing(cfg)
+    w = GpuWeights(cfg)
+    bad = routing[0].copy()
+    bad[5, 0] = cfg.E + 3                             # outside [-1, E): the routing kernel rejects it
+    _noalloc(cfg, w, GpuTokens(cfg, routing=(bad, routing[1], 0.0)))
+    st, sm, info = mm.mm_noalloc_get_status()
+    assert st == mm.MM_ERR_BAD_INDEX and info == 5 * cfg.k + 0, (mm.STATUS_NAMES.get(st, st), info)
+    tok = GpuTokens(cfg, routing=routing)
+    got = _noalloc(cfg, w, tok)
+    assert mm.mm_noalloc_get_status()[0] == mm.MM_OK   # the next call reset the status
+    want = _with_workspace(cfg, w, tok)
+    assert torch.equal(got.view(torch.int16), want.view(torch.int16))
+    assert np.all(np.isfinite(bf16_to_np(got)))
 
 
 def test_noalloc_refuses_shapes_beyond_its_scratch():
