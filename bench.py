@@ -218,6 +218,7 @@ def replica_throughput(ms_local, tokens_per_rank, world, max_over_ranks):
 
 # ------------------------------------------------------------------ our arm
 PER_CONFIG = ("prefill", "skew", "kimi")       # timed after the headline in the same run (1 GPU)
+PAIR_CONFIG = ("prefill",)                     # also timed with the two-CTA tiles switched on
 
 
 def _quant(mm, src, rows, cols, fmt, out, out_sf):
@@ -446,6 +447,7 @@ def run_ours(args, rank, world, local_rank):
 
     roofline = _roofline(cfg, ms, idx_np, bf16_layer, args.workload,
                          "whole step: routing + megamoe_kernel + combine_kernel", route_ms)
+    roofline["layer_kernel"] = mm.VARIANT_NAMES.get(mm.mm_layer_variant(T, E, k, H, bf16_layer))
     launches_per_step = (1 if T * k <= 2048 else 3) + 2
 
     # ---- the other full-size configurations, timed the same way (1 GPU only)
@@ -462,10 +464,19 @@ def run_ours(args, rank, world, local_rank):
                 l1_w, l1_sf, l2_w, l2_sf = _make_weights(mm, synth, torch, pc, dev, False)
                 weights = (l1_w, l1_sf, l2_w, l2_sf)
                 E, H, I = pc.E, pc.H, pc.I
-            per_config[name] = _time_config(mm, synth, torch, np, pc, weights, dev, stream, uuid, local_rank,
-                                            args.per_config_steps, max(3, args.warmup))
-            launches_per_step_pc = (1 if pc.T * pc.k <= 2048 else 3) + 2
-            per_config[name]["gpu_launches"] = launches_per_step_pc * per_config[name]["steps"]
+            runs = [(name, None)] + ([(f"{name} (two-CTA tiles)", 1)] if name in args.pair_config else [])
+            for key, pair in runs:
+                prev = mm.mm_set_pair_mma(pair) if pair is not None else None
+                try:
+                    per_config[key] = _time_config(mm, synth, torch, np, pc, weights, dev, stream, uuid, local_rank,
+                                                   args.per_config_steps, max(3, args.warmup))
+                finally:
+                    if prev is not None:
+                        mm.mm_set_pair_mma(prev)
+                per_config[key]["layer_kernel"] = mm.VARIANT_NAMES.get(
+                    mm.mm_layer_variant(pc.T, pc.E, pc.k, pc.H) if pair is None else 4)
+                launches_per_step_pc = (1 if pc.T * pc.k <= 2048 else 3) + 2
+                per_config[key]["gpu_launches"] = launches_per_step_pc * per_config[key]["steps"]
     return {
         "tokens_per_s": tokens_per_s, "ms": ms, "route_ms": route_ms, "roofline": roofline,
         "e2e": {"value": round(e2e_tps, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
@@ -604,11 +615,14 @@ def main():
     ap.add_argument("--per-config", default=",".join(PER_CONFIG),
                     help="full-size configurations timed after the headline (1 GPU); empty for none")
     ap.add_argument("--per-config-steps", type=int, default=20)
+    ap.add_argument("--pair-config", default=",".join(PAIR_CONFIG),
+                    help="per-config workloads also timed with the two-CTA tiles switched on")
     ap.add_argument("--tokens", type=int, default=0, help="override the token count (profiling of small cases)")
     ap.add_argument("--experts", type=int, default=0, help="override the expert count (profiling of small cases)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     args.per_config = [c for c in args.per_config.split(",") if c and c != args.workload]
+    args.pair_config = [c for c in args.pair_config.split(",") if c]
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))

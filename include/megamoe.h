@@ -192,6 +192,36 @@ int mm_set_reserved_sms(int n);
 int mm_get_reserved_sms(void);
 
 /*
+ * mm_set_pair_mma -- whether mm_forward and mm_forward_bf16 run batches of
+ * more than 16 assignments per expert (on average) as MMA tiles of 256 tokens
+ * shared by a cluster of two CTAs on neighbouring SMs (tcgen05 cta_group::2:
+ * M = 256, each CTA loading and holding half of the tile's 256 weight rows),
+ * or as 128-token tiles of one CTA.  The pages' kernel runs an even grid of
+ * such two-CTA clusters ([P1] Root cause and Fix: the reserve keeps the grid
+ * even so that it stays "compatible with the two-CTA cluster").  Applies only
+ * when hidden is a multiple of 256 (every weight tile then splits into two
+ * 128-row halves); other shapes, decode-sized batches and mm_bf16_forward use
+ * one-CTA tiles.  The result is the same either way (same arithmetic, same
+ * rounding).  enable != 0 turns it on.  Process-wide; read at each launch.
+ * Returns the previous value.  Off by default: on GB300 the two-CTA tiles
+ * measured slower than the one-CTA tiles (about 1.85x the step time of the
+ * 8192-token batch).  The environment variable MM_PAIR_MMA (0 or 1), if set
+ * when the library first needs it, replaces the default of 0.
+ */
+int mm_set_pair_mma(int enable);
+int mm_get_pair_mma(void);
+
+/*
+ * mm_layer_variant -- which layer kernel a launch of this shape runs, under
+ * the current settings: 0 one-CTA tiles of 128 tokens, 1 one-CTA tiles of
+ * 32-token stages (at most 16 assignments per expert on average), 2 and 3 the
+ * same two for mm_bf16_forward (bf16_layer != 0), 4 two-CTA tiles of 256
+ * tokens (see mm_set_pair_mma).  MM_ERR_INVALID_ARG for a bad shape.  Host
+ * only; for tests and reports.
+ */
+int mm_layer_variant(int num_tokens, int experts, int topk, int hidden, int bf16_layer);
+
+/*
  * mm_grid_size -- the launch-size rule, exposed for tests and callers:
  *   cap    = max(2, device_sms - max(reserved_sms, 0))
  *   want   = num_sms > 0 ? min(num_sms, device_sms) : device_sms

@@ -41,6 +41,9 @@ _SIGS = {
     "mm_forward": (_c_int, [_c_int] * 5 + [_c_vp] * 9 + [ctypes.c_float, _c_int, _c_vp, _c_size, _c_vp]),
     "mm_set_reserved_sms": (_c_int, [_c_int]),
     "mm_get_reserved_sms": (_c_int, []),
+    "mm_set_pair_mma": (_c_int, [_c_int]),
+    "mm_get_pair_mma": (_c_int, []),
+    "mm_layer_variant": (_c_int, [_c_int] * 5),
     "mm_grid_size": (_c_int, [_c_int] * 4),
     "mm_set_wait_timeout_ns": (None, [ctypes.c_ulonglong]),
     "mm_get_wait_timeout_ns": (ctypes.c_ulonglong, []),
@@ -140,6 +143,23 @@ def mm_set_reserved_sms(n) -> int:
 
 def mm_get_reserved_sms() -> int:
     return lib().mm_get_reserved_sms()
+
+
+def mm_set_pair_mma(enable) -> int:
+    """Two-CTA (M = 256) tiles for wide batches on (1) or off (0); returns the previous setting."""
+    return lib().mm_set_pair_mma(int(enable))
+
+
+def mm_get_pair_mma() -> int:
+    return lib().mm_get_pair_mma()
+
+
+VARIANT_NAMES = {0: "wide (one CTA, 128-token tiles)", 1: "thin (one CTA, 32-token stages)",
+                 2: "bf16 wide", 3: "bf16 thin", 4: "pair (two CTAs, 256-token tiles)"}
+
+
+def mm_layer_variant(num_tokens, experts, topk, hidden, bf16_layer=False) -> int:
+    return lib().mm_layer_variant(num_tokens, experts, topk, hidden, int(bool(bf16_layer)))
 
 
 def mm_grid_size(device_sms, reserved_sms, num_sms, max_resident=0) -> int:

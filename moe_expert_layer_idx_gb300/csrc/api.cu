@@ -15,7 +15,7 @@ __global__ void route_count_kernel(const RouteParams p);
 __global__ void route_scan_kernel(const RouteParams p);
 __global__ void route_scatter_kernel(const RouteParams p);
 int layer_max_rows(int variant);
-cudaError_t layer_prepare(int variant, int* ctas_per_sm);
+cudaError_t layer_prepare(int variant, int sms, int* resident);
 cudaError_t layer_launch(int variant, int grid, cudaStream_t stream, const CUtensorMap* maps, const ForwardParams& p);
 cudaError_t launch_quantize(const float* src, long long nblocks, bool e4m3, uint8_t* dst, uint8_t* sf,
                             int grid, cudaStream_t stream);
@@ -27,9 +27,11 @@ namespace {
 
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;
 constexpr int kDefaultReserve = 2;   // sglang PR #36657, Summary: two SMs by default
+constexpr int kDefaultPair = 0;      // two-CTA tiles measured slower than one-CTA tiles: off unless switched on
 
 std::atomic<int> g_reserved{-1};
 std::atomic<unsigned long long> g_timeout_ns{kDefaultTimeoutNs};
+std::atomic<int> g_pair{-1};       // two-CTA MMA tiles for wide batches: -1 = not yet read from the environment
 
 int reserved_now() {
   int r = g_reserved.load();
@@ -43,6 +45,20 @@ int reserved_now() {
   int expected = -1;
   g_reserved.compare_exchange_strong(expected, v);
   return g_reserved.load();
+}
+
+int pair_now() {
+  int v = g_pair.load();
+  if (v >= 0) return v;
+  v = kDefaultPair;
+  if (const char* env = std::getenv("MM_PAIR_MMA")) {
+    char* end = nullptr;
+    long x = std::strtol(env, &end, 10);
+    if (end != env) v = x != 0 ? 1 : 0;
+  }
+  int expected = -1;
+  g_pair.compare_exchange_strong(expected, v);
+  return g_pair.load();
 }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -66,12 +82,15 @@ struct DevState {
 };
 
 // Kernel variant for a batch: with at most 16 assignments per expert on
-// average (decode), the thin variant's deeper weight ring; otherwise the wide
-// variant's 128-token tiles.
-int pick_variant(long long assignments, int experts, bool bf16_layer) {
+// average (decode), the thin variant's deeper weight ring; otherwise 128-token
+// tiles, or 256-token tiles on a pair of CTAs (FP8 x FP4 layer, hidden size a
+// multiple of 256 so that every L2 weight block splits into two 128-row
+// halves, and the pair switch on).
+int pick_variant(long long assignments, int experts, int hidden, bool bf16_layer) {
   const bool thin = assignments <= 16ll * experts;
   if (bf16_layer) return thin ? kVariantBf16Thin : kVariantBf16Wide;
-  return thin ? kVariantThin : kVariantWide;
+  if (thin) return kVariantThin;
+  return (hidden % 256 == 0 && pair_now()) ? kVariantPair : kVariantWide;
 }
 std::mutex g_mu;
 DevState g_dev[128];
@@ -110,12 +129,12 @@ int device_state(int* dev_out, DevState** st_out) {
       return MM_ERR_CUDA;
     }
     for (int v = 0; v < kNumVariants; ++v) {
-      int per_sm = 0;
-      if (layer_prepare(v, &per_sm) != cudaSuccess) {
+      int resident = 0;
+      if (layer_prepare(v, prop.multiProcessorCount, &resident) != cudaSuccess) {
         cudaGetLastError();
         return MM_ERR_CUDA;
       }
-      st.max_resident[v] = per_sm * prop.multiProcessorCount;
+      st.max_resident[v] = resident;
     }
     st.sms = prop.multiProcessorCount;
     st.ready = true;
@@ -137,12 +156,14 @@ int encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t
   return r == CUDA_SUCCESS ? MM_OK : MM_ERR_CUDA;
 }
 
-int launch_route(int T, int E, int k, const int32_t* topk_idx, uint8_t* ws, const Layout& L, cudaStream_t st) {
+// `variant`: the layer kernel that consumes the routing (its largest token block).
+int launch_route(int T, int E, int k, int variant, const int32_t* topk_idx, uint8_t* ws, const Layout& L,
+                 cudaStream_t st) {
   RouteParams rp;
   rp.T = T; rp.E = E; rp.k = k; rp.A = T * k;
   rp.C = route_ctas(rp.A);
   rp.chunk = (rp.A + rp.C - 1) / rp.C;
-  rp.max_n = layer_max_rows(pick_variant((long long)T * k, E, false));   // the same rows for both layers
+  rp.max_n = layer_max_rows(variant);   // the same token blocks for both layers
   rp.topk_idx = topk_idx;
   rp.ws = ws;
   rp.L = L;
@@ -184,6 +205,19 @@ int mm_set_reserved_sms(int n) {
 }
 
 int mm_get_reserved_sms(void) { return reserved_now(); }
+
+int mm_set_pair_mma(int enable) {
+  const int prev = pair_now();
+  g_pair.store(enable != 0 ? 1 : 0);
+  return prev;
+}
+
+int mm_get_pair_mma(void) { return pair_now(); }
+
+int mm_layer_variant(int num_tokens, int experts, int topk, int hidden, int bf16_layer) {
+  if (num_tokens < 0 || experts < 1 || topk < 1) return MM_ERR_INVALID_ARG;
+  return pick_variant((long long)num_tokens * topk, experts, hidden, bf16_layer != 0);
+}
 
 int mm_grid_size(int device_sms, int reserved_sms, int num_sms, int max_resident) {
   if (device_sms < 2) return MM_ERR_INVALID_ARG;
@@ -236,7 +270,7 @@ static int forward_impl(bool bf16_layer, int num_tokens, int experts, int topk, 
   DevState* st;
   rc = device_state(&dev, &st);
   if (rc != MM_OK) return rc;
-  const int variant = pick_variant((long long)T * k, E, bf16_layer);
+  const int variant = pick_variant((long long)T * k, E, H, bf16_layer);
   const int grid = mm_grid_size(st->sms, reserved_now(), num_sms, st->max_resident[variant]);
   const int A = T * k;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -269,7 +303,7 @@ static int forward_impl(bool bf16_layer, int num_tokens, int experts, int topk, 
     return MM_ERR_CUDA;
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  rc = launch_route(T, E, k, topk_idx, ws, L, s);
+  rc = launch_route(T, E, k, variant, topk_idx, ws, L, s);
   if (rc != MM_OK) return rc;
 
   ForwardParams fp;
@@ -336,8 +370,8 @@ int mm_route(int num_tokens, int experts, int topk, int hidden, int inter, const
   DevState* st;
   rc = device_state(&dev, &st);
   if (rc != MM_OK) return rc;
-  return launch_route(num_tokens, experts, topk, topk_idx, static_cast<uint8_t*>(workspace), L,
-                      reinterpret_cast<cudaStream_t>(stream));
+  return launch_route(num_tokens, experts, topk, pick_variant((long long)num_tokens * topk, experts, hidden, false),
+                      topk_idx, static_cast<uint8_t*>(workspace), L, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int mm_read_routing(int num_tokens, int experts, int topk, int hidden, int inter, const void* workspace,

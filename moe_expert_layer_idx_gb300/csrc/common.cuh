@@ -60,7 +60,16 @@ constexpr uint32_t kSFSetCols = 12;                 // SFA: +0..3, SFB: +4..11
 // kSub: K sub-stages (128 wide each, or 64 for bf16) per ring slot.  A slot is
 // one full/empty barrier round trip; two sub-stages per slot halve the round
 // trips, waits and commits per weight byte at the same bytes in flight.
-template <int kARows_, int kStages_, bool kXpose_, bool kBf16_, int kSub_ = 1>
+//
+// kPair: a cluster of two CTAs on neighbouring SMs computes each tile with
+// one MMA of M = 256 (tcgen05 cta_group::2): up to 256 tokens of one expert,
+// 128 per CTA, times the tile's 256 weight rows, of which each CTA loads and
+// holds 128.  A CTA's stage then carries half the weight bytes, so the ring
+// can be half again as deep, and each weight row is read once per 256 tokens
+// instead of once per 128.  The even CTA of the pair issues every MMA; the
+// odd one loads its share, writes its scale atoms and runs the epilogue of
+// its 128 accumulator rows.
+template <int kARows_, int kStages_, bool kXpose_, bool kBf16_, int kSub_ = 1, bool kPair_ = false>
 struct Variant {
   static constexpr int kARows = kARows_;
   static constexpr int kStages = kStages_;            // ring slots
@@ -68,17 +77,22 @@ struct Variant {
   static_assert(kSub == 1 || kSub == 2, "sub-stages per slot");
   static constexpr bool kXpose = kXpose_;
   static constexpr bool kBf16 = kBf16_;
+  static constexpr bool kPair = kPair_;
+  static_assert(!kPair || (!kBf16 && kARows == kTileM && kSub == 1), "the pair variant is the wide FP8 x FP4 one");
+  static constexpr int kCtas = kPair ? 2 : 1;          // CTAs that share one MMA tile
+  static constexpr int kBlockRows = kARows * kCtas;    // largest token block of a tile
   static constexpr int kKStage = kBf16 ? kBlockK / 2 : kBlockK;     // K elements per stage
   static constexpr int kWeightBoxTx = kBf16 ? 128 * 128 : kBHalfTxBytes;   // one 128-row weight box
   static constexpr int kABytes = kARows * kBlockK;
-  static constexpr int kStageBytes = kABytes + kBBytes + kSFABytes + kSFBBytes;
+  static constexpr int kBStageBytes = kPair ? kBBytes / 2 : kBBytes;       // weight rows this CTA holds
+  static constexpr int kStageBytes = kABytes + kBStageBytes + kSFABytes + kSFBBytes;
   // Epilogue transpose buffer per warp: 32 token rows x 16 fp32 columns, so the
   // L2 epilogue stores whole 64-byte row segments instead of 16-byte pieces of
   // 32 different rows.
   static constexpr int kXposeBytes = kXpose ? kEpiWarps * 32 * 16 * 4 : 0;
   static constexpr int kSmemBytes = kStages * kSub * kStageBytes + kXposeBytes + kBarBytes + 1024 /*align*/;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
-  static_assert(kABytes % 1024 == 0 && kBBytes % 1024 == 0, "SW128 tiles need 1 KB alignment");
+  static_assert(kABytes % 1024 == 0 && kBStageBytes % 1024 == 0, "SW128 tiles need 1 KB alignment");
   static_assert(kARows % 16 == 0 && kARows <= kTileM, "token rows per stage");
   // barriers (2 per stage, 3 accumulator/drain, 2 per tile-ring slot), misc words, votes, tile ring
   static_assert((2 * kStages + 3 + 2 * kTileRing) * 8 + 8 * 4 + 2 * kEpiWarps * 4 + kTileRing * 9 * 4 <= kBarBytes,
@@ -91,8 +105,9 @@ using WideVariant = Variant<128, 4, true, false>;
 using ThinVariant = Variant<32, 3, false, false, 2>;
 using Bf16WideVariant = Variant<128, 4, true, true>;
 using Bf16ThinVariant = Variant<32, 6, false, true>;
+using PairVariant = Variant<128, 6, true, false, 1, true>;
 enum VariantId : int {
-  kVariantWide = 0, kVariantThin = 1, kVariantBf16Wide = 2, kVariantBf16Thin = 3, kNumVariants = 4
+  kVariantWide = 0, kVariantThin = 1, kVariantBf16Wide = 2, kVariantBf16Thin = 3, kVariantPair = 4, kNumVariants = 5
 };
 
 
@@ -251,13 +266,23 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
 __device__ __forceinline__ void fence_mbar_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
+// kCluster: acquire at cluster scope, for a phase completed by arrivals from
+// the other CTA of a pair (its shared-memory writes become visible).
+template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+  if constexpr (kCluster)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+  else
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
   return ok != 0;
 }
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
@@ -269,12 +294,13 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
 
 // Bounded wait on an mbarrier phase: polls the abort flag and the global timer.
 // Returns false if the time limit passed or another thread raised the abort flag.
+template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t* ctrl,
                                           unsigned long long timeout_ns, uint32_t site) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_try_wait<kCluster>(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   uint32_t it = 0;
-  while (!mbar_try_wait(bar, parity)) {
+  while (!mbar_try_wait<kCluster>(bar, parity)) {
     if ((++it & 63u) == 0u) {
       if (ld_volatile(&ctrl[kAbort]) != 0u) return false;
       if (globaltimer() - t0 > timeout_ns) {
@@ -297,6 +323,44 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, u
     if ((++it & 63u) == 0u && globaltimer() - t0 > timeout_ns) return false;
   }
   return true;
+}
+
+// ---- clusters of two CTAs (the pair variant)
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Address in the cluster's shared window of the variable at `saddr` (this
+// CTA's shared address) in the CTA of rank `rank`.
+__device__ __forceinline__ uint32_t cluster_addr(uint32_t saddr, uint32_t rank) {
+  uint32_t d;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(saddr), "r"(rank));
+  return d;
+}
+// Every thread of both CTAs: orders each CTA's earlier memory operations
+// (including remote ones) before the other's later ones.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Arrive on an mbarrier of either CTA (cluster address); release at cluster
+// scope orders this thread's earlier shared-memory writes before it.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cl) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" :: "r"(bar_cl) : "memory");
+}
+// Arrive with an expected transaction count; relaxed (it announces TMA bytes
+// only, it publishes no data of its own).
+__device__ __forceinline__ void mbar_arrive_expect_tx_cluster(uint32_t bar_cl, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.relaxed.cluster.shared::cluster.b64 _, [%0], %1;"
+               :: "r"(bar_cl), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void st_cluster_u32(uint32_t addr_cl, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" :: "r"(addr_cl), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t addr_cl) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr_cl) : "memory");
+  return v;
 }
 
 // Bounded wait until a global counter reaches `target` (acquire).
@@ -327,47 +391,98 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
       : "memory");
 }
+// TMA into this CTA's shared memory, completing on a barrier of either CTA of
+// a pair (cluster address): the pair's loads all land on the leader's barrier.
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar_cl,
+                                                 int32_t x, int32_t y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];"
+      :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cl)
+      : "memory");
+}
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
-// ---- tcgen05
+// ---- tcgen05.  G = 1: one CTA; G = 2: a pair of CTAs (cluster of two) that
+// allocate TMEM together and whose MMAs the even CTA issues for both: operand
+// A rows 0-127 and B rows 0..N/2-1 from the even CTA's shared memory, the
+// rest from the odd CTA's at the same offsets; each CTA's TMEM receives its
+// own 128 accumulator rows; scale copies fill both CTAs' TMEM from their own
+// shared memory, and the B scales must cover all N in both.
+template <int G = 1>
 __device__ __forceinline__ void tc_alloc(uint32_t dst_smem, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" :: "r"(dst_smem), "r"(ncols) : "memory");
+  if constexpr (G == 2)
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" :: "r"(dst_smem), "r"(ncols) : "memory");
+  else
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" :: "r"(dst_smem), "r"(ncols) : "memory");
 }
+template <int G = 1>
 __device__ __forceinline__ void tc_relinquish() {
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  if constexpr (G == 2) asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  else asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
 }
+template <int G = 1>
 __device__ __forceinline__ void tc_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(taddr), "r"(ncols) : "memory");
+  if constexpr (G == 2)
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" :: "r"(taddr), "r"(ncols) : "memory");
+  else
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(taddr), "r"(ncols) : "memory");
 }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+// Arrive on `bar` (a shared address of this CTA, or a cluster address of
+// either CTA of a pair) once this thread's earlier MMAs and copies are done.
+template <int G = 1>
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" :: "r"(bar) : "memory");
+  if constexpr (G == 2)
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" :: "r"(bar) : "memory");
+  else
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" :: "r"(bar) : "memory");
 }
 // Copy a 32-row x 16-byte scale atom from shared memory to 4 TMEM columns,
 // replicated to the four 32-lane quarters.
+template <int G = 1>
 __device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t src_desc) {
-  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" :: "r"(taddr), "l"(src_desc) : "memory");
+  if constexpr (G == 2)
+    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" :: "r"(taddr), "l"(src_desc) : "memory");
+  else
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" :: "r"(taddr), "l"(src_desc) : "memory");
 }
 // D (+)= (A * 2^sfa) . (B * 2^sfb)^T, block-scaled, one scale per 32 K.
+template <int G = 1>
 __device__ __forceinline__ void tc_mma_mx(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                           uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %6, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
-      :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
-      : "memory");
+  if constexpr (G == 2)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+        :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+  else
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+        :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
 }
 // Same, always accumulating into D.
+template <int G = 1>
 __device__ __forceinline__ void tc_mma_mx_acc(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                               uint32_t sfa_tmem, uint32_t sfb_tmem) {
-  asm volatile(
-      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], 1;"
-      :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem)
-      : "memory");
+  if constexpr (G == 2)
+    asm volatile(
+        "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], 1;"
+        :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem)
+        : "memory");
+  else
+    asm volatile(
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], 1;"
+        :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem)
+        : "memory");
 }
 // 32 lanes x 16 columns of 32-bit accumulators into registers.
 __device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16]) {
@@ -404,16 +519,16 @@ __device__ __forceinline__ uint64_t desc_sf(uint32_t saddr) {
   return d;
 }
 // Instruction descriptor of kind::mxf8f6f4 with UE8M0 scales: A = E4M3 tokens
-// (M = 128), B = E2M1 weights (N), both K-major; sf_id selects the scale byte
-// (the 32-element K block within the 128-element stage).
-__device__ __forceinline__ uint32_t idesc_mx(uint32_t n, uint32_t sf_id) {
+// (M = 128, or 256 over a pair), B = E2M1 weights (N), both K-major; sf_id
+// selects the scale byte (the 32-element K block within the 128-element stage).
+__device__ __forceinline__ uint32_t idesc_mx(uint32_t n, uint32_t sf_id, uint32_t m = 128) {
   uint32_t d = 0;
   d |= sf_id << 4;                 // B scale-factor id
   d |= 0u << 7;                    // A format: E4M3
   d |= 5u << 10;                   // B format: E2M1
   d |= (n >> 3) << 17;             // N / 8
   d |= 1u << 23;                   // scale format: UE8M0
-  d |= (128u >> 4) << 24;          // M / 16
+  d |= (m >> 4) << 24;             // M / 16
   d |= sf_id << 29;                // A scale-factor id
   return d;
 }

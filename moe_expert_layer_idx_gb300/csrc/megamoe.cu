@@ -112,13 +112,39 @@ __device__ __forceinline__ void decode_tile(int t, int nL1, const ForwardParams&
 // unfinished L1 tile is always either running or held (claimed ahead) by a CTA
 // whose running tile is an L1 tile or an L2 tile of a larger index: no cycle of
 // waits can form.
+// In a pair, the even CTA's producer 0 claims for both: it also writes each
+// tile into the odd CTA's ring and arrives on that ring's barrier; the odd
+// CTA's readers take tiles from their own ring (acquiring at cluster scope)
+// and free the slot on the even CTA's barrier, which counts both CTAs' readers.
 struct TileFeed {
   Tile* ring;
   uint64_t* full;
   uint64_t* empty;
   uint32_t i = 0;
   int ahead = -1;              // producer 0: index claimed for the next publication
+  bool peer = false;           // a reader of the odd CTA of a pair
+  uint32_t empty_cl = 0;       // odd CTA: cluster address of the even CTA's empty[0]
+  uint32_t peer_ring_cl = 0;   // even CTA's producer 0: the odd CTA's ring[0] and full[0]
+  uint32_t peer_full_cl = 0;
   __device__ TileFeed(Tile* r, uint64_t* f, uint64_t* e) : ring(r), full(f), empty(e) {}
+  // The pair's wiring: rank 0 publishes to rank 1; rank 1 frees rank 0's slots.
+  __device__ void pair(uint32_t rank) {
+    if (rank == 0) {
+      peer_ring_cl = cluster_addr(smem_u32(ring), 1);
+      peer_full_cl = cluster_addr(smem_u32(full), 1);
+    } else {
+      peer = true;
+      empty_cl = cluster_addr(smem_u32(empty), 0);
+    }
+  }
+  __device__ bool wait_full(uint32_t slot, uint32_t ph, uint32_t* ctrl, unsigned long long to) {
+    return peer ? mbar_wait<true>(smem_u32(&full[slot]), ph, ctrl, to, kSiteTileRing << 24)
+                : mbar_wait(smem_u32(&full[slot]), ph, ctrl, to, kSiteTileRing << 24);
+  }
+  __device__ void release(uint32_t slot) {
+    if (peer) mbar_arrive_cluster(empty_cl + 8u * slot);
+    else mbar_arrive(smem_u32(&empty[slot]));
+  }
 
   // Producer 0: claim, decode, publish.  Returns false at the end of the stream or on abort (ok = false).
   __device__ bool claim(uint32_t* counter, int total, int nL1, const ForwardParams& p, const int32_t* items,
@@ -126,11 +152,17 @@ struct TileFeed {
                         bool& ok, Tile& ti) {
     const uint32_t slot = i % kTileRing, ph = (i / kTileRing) & 1u;
     ++i;
-    if (!mbar_wait(smem_u32(&empty[slot]), ph ^ 1u, ctrl, to, kSiteTileRing << 24)) { ok = false; return false; }
+    if (!mbar_wait<true>(smem_u32(&empty[slot]), ph ^ 1u, ctrl, to, kSiteTileRing << 24)) { ok = false; return false; }
     const int t = ahead >= 0 ? ahead : (int)atomicAdd(counter, 1u);
     if (t < total) decode_tile(t, nL1, p, items, counts, offsets, ti);
     else ti.layer = 0;
     ring[slot] = ti;
+    if (peer_ring_cl != 0) {
+      const uint32_t* w = reinterpret_cast<const uint32_t*>(&ti);
+#pragma unroll
+      for (int q = 0; q < (int)(sizeof(Tile) / 4); ++q) st_cluster_u32(peer_ring_cl + slot * sizeof(Tile) + 4 * q, w[q]);
+      mbar_arrive_cluster(peer_full_cl + 8u * slot);   // release: the remote writes come first
+    }
     mbar_arrive(smem_u32(&full[slot]));          // release: the tile is visible to the readers
     ahead = t < total ? (int)atomicAdd(counter, 1u) : -1;   // consumed at the next claim
     return ti.layer != 0;
@@ -139,9 +171,9 @@ struct TileFeed {
   __device__ bool take(uint32_t* ctrl, unsigned long long to, bool& ok, Tile& ti) {
     const uint32_t slot = i % kTileRing, ph = (i / kTileRing) & 1u;
     ++i;
-    if (!mbar_wait(smem_u32(&full[slot]), ph, ctrl, to, kSiteTileRing << 24)) { ok = false; return false; }
+    if (!wait_full(slot, ph, ctrl, to)) { ok = false; return false; }
     ti = ring[slot];
-    mbar_arrive(smem_u32(&empty[slot]));
+    release(slot);
     return ti.layer != 0;
   }
   // A whole warp: lane 0 waits, every lane then observes the completed phase
@@ -151,13 +183,14 @@ struct TileFeed {
     const uint32_t slot = i % kTileRing, ph = (i / kTileRing) & 1u;
     ++i;
     bool w = true;
-    if (lane == 0) w = mbar_wait(smem_u32(&full[slot]), ph, ctrl, to, kSiteTileRing << 24);
+    if (lane == 0) w = wait_full(slot, ph, ctrl, to);
     w = __shfl_sync(0xffffffffu, w, 0);
     if (!w) { ok = false; return false; }
-    (void)mbar_try_wait(smem_u32(&full[slot]), ph);
+    if (peer) (void)mbar_try_wait<true>(smem_u32(&full[slot]), ph);
+    else (void)mbar_try_wait(smem_u32(&full[slot]), ph);
     ti = ring[slot];
     __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&empty[slot]));
+    if (lane == 0) release(slot);
     return ti.layer != 0;
   }
 };
@@ -185,7 +218,7 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
   constexpr int kSubs = kStages * kSub;
   uint8_t* sA = sm;                                   // [kSubs] token rows
   uint8_t* sB = sA + kSubs * kABytes;                 // [kSubs] weight rows
-  uint8_t* sSFA = sB + kSubs * kBBytes;               // [kSubs] token scale atom
+  uint8_t* sSFA = sB + kSubs * V::kBStageBytes;       // [kSubs] token scale atom
   uint8_t* sSFB = sSFA + kSubs * kSFABytes;           // [kSubs] two weight scale atoms
   float* sX = reinterpret_cast<float*>(sSFB + kSubs * kSFBBytes);   // [kEpiWarps] transpose buffers
   uint64_t* bars = reinterpret_cast<uint64_t*>(sSFB + kSubs * kSFBBytes + V::kXposeBytes);
@@ -196,15 +229,25 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
   uint64_t* drain = tempty + 1;              // final MMA drain
   uint64_t* tile_full = drain + 1;           // [kTileRing] tile index published
   uint64_t* tile_empty = tile_full + kTileRing;   // [kTileRing] read by every consumer role
-  // tmem base, stages consumed (MMA), stages issued (producer 0), (unused), stages armed (scale
-  // loader), stages issued (producer 1)
+  // tmem base, stages consumed (MMA), stages issued (producer 0), status read at the start, stages
+  // armed (scale loader), stages issued (producer 1)
   uint32_t* s_misc = reinterpret_cast<uint32_t*>(tile_empty + kTileRing);
   int32_t* s_vote = reinterpret_cast<int32_t*>(s_misc + 8);    // epilogue votes [2][kEpiWarps]
   Tile* s_tiles = reinterpret_cast<Tile*>(s_vote + 2 * kEpiWarps);   // [kTileRing] claimed tiles
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int G = V::kCtas;                     // CTA group of every tcgen05 instruction
+  const uint32_t crank = V::kPair ? cluster_rank() : 0u;
+  const bool leader = crank == 0;                 // the CTA that issues the MMAs
   uint32_t* ctrl = reinterpret_cast<uint32_t*>(p.ws + p.L.ctrl);
-  if (ld_volatile(&ctrl[kStatus]) != 0u) return;   // routing rejected the input
+  // A nonzero status (the routing rejected the input) ends the launch.  The
+  // two CTAs of a pair must take the same decision, because each blocks in the
+  // collective TMEM allocation and the cluster barriers until the other comes:
+  // they both go through the prologue and follow the even CTA's reading.
+  const uint32_t status0 = ld_volatile(&ctrl[kStatus]);
+  if constexpr (!V::kPair) {
+    if (status0 != 0u) return;
+  }
 
   const int32_t* counts = reinterpret_cast<const int32_t*>(p.ws + p.L.counts);
   const int32_t* offsets = reinterpret_cast<const int32_t*>(p.ws + p.L.offsets);
@@ -221,17 +264,19 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], V::kBf16 ? 2 : 2 + 1);      // producers (+ the scale loader)
+      // producers (+ the scale loader), of both CTAs of a pair
+      mbar_init(&full[s], (V::kBf16 ? 2 : 2 + 1) * G);
       mbar_init(&empty[s], 1);
     }
     mbar_init(tfull, 1);
-    mbar_init(tempty, kEpiWarps);
+    mbar_init(tempty, kEpiWarps * G);
     mbar_init(drain, 1);
     for (int i = 0; i < kTileRing; ++i) {
       mbar_init(&tile_full[i], 1);
-      mbar_init(&tile_empty[i], kTileReaders);
+      mbar_init(&tile_empty[i], kTileReaders * G);   // a pair's odd CTA has as many readers as the even one
     }
     for (int i = 1; i < 8; ++i) s_misc[i] = 0;
+    s_misc[3] = status0;                        // read by the odd CTA of a pair
     fence_mbar_init();
     prefetch_tensormap(&tm_w1);
     prefetch_tensormap(&tm_w2);
@@ -241,13 +286,17 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
     prefetch_tensormap(&tm_l1a128);
   }
   if (warp == 1) {
-    tc_alloc(smem_u32(&s_misc[0]), kTmemCols);
-    tc_relinquish();
+    tc_alloc<G>(smem_u32(&s_misc[0]), kTmemCols);   // a pair allocates in both CTAs together
+    tc_relinquish<G>();
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (V::kPair) cluster_sync();          // both CTAs' barriers exist before any remote arrival
   tc_fence_after();
   const uint32_t tmem = s_misc[0];
+  bool skip = false;                               // (outside a pair the status was checked above)
+  if constexpr (V::kPair) skip = ld_cluster_u32(cluster_addr(smem_u32(&s_misc[3]), 0)) != 0u;
+  if (!skip) {
 
   // ------------------------------------------------------------ 0. dispatch
   if (!V::kBf16 && p.x_bf16 != nullptr) {
@@ -367,15 +416,21 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
       // tile (L1: the gate rows, then the up rows) and the 16-row token boxes j
       // with j % 2 == pid (a single 128-row token box goes to producer 0), and
       // arms the stage's barrier with its own bytes.
+      // In a pair, CTA r loads token rows [128r, 128r + 128) of the block and
+      // weight rows [128r, 128r + 128) of the tile (one box, producer 0; a
+      // single 128-row token box goes to producer 1), and every load of both
+      // CTAs completes on the even CTA's barrier.
       const int pid = warp == 0 ? 0 : 1;
       uint32_t stage = 0, phase = 0, issued = 0;
       int ready_key = -1;            // (layer, expert) whose dependency was last seen satisfied
       bool ok = true;
       TileFeed feed(s_tiles, tile_full, tile_empty);
+      if constexpr (V::kPair) feed.pair(crank);
+      const bool claimer = pid == 0 && leader;
       while (ok) {
         Tile ti;
-        const bool more = pid == 0 ? feed.claim(&ctrl[kNextTile], total, nL1, p, items, counts, offsets, ctrl, to, ok, ti)
-                                   : feed.take(ctrl, to, ok, ti);
+        const bool more = claimer ? feed.claim(&ctrl[kNextTile], total, nL1, p, items, counts, offsets, ctrl, to, ok, ti)
+                                  : feed.take(ctrl, to, ok, ti);
         if (!more) break;
         const uint32_t tag = (uint32_t)ti.tag;
         const int key = ti.e * 2 + ti.layer - 1;
@@ -383,36 +438,49 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
           if (ti.layer == 1)
             ok = counter_wait(&arrival[ti.e], (uint32_t)__ldg(counts + ti.e), ctrl, to, (kSiteArrival << 24) | tag);
           else
-            ok = counter_wait(&l1_done[ti.e], l1_tiles_of(items, ti.e, p.mt1), ctrl, to, (kSiteL1Done << 24) | tag);
+            ok = counter_wait(&l1_done[ti.e], G * l1_tiles_of(items, ti.e, p.mt1), ctrl, to,
+                              (kSiteL1Done << 24) | tag);
           if (!ok) break;
           fence_proxy_async_global();
           ready_key = key;
         }
-        const bool full_box = V::kARows == kTileM && p.a_box128 && ti.m16 == kTileM;
-        const int nbox = ti.m16 / 16;
-        const int my_a_bytes = full_box ? (pid == 0 ? kABytes : 0) : ((nbox + 1 - pid) / 2) * 16 * kBlockK;
-        const bool my_b = pid == 0 || ti.n > 128;
+        const int tr = (int)crank * kTileM;                       // this CTA's first row of the block
+        const int rows = max(0, min(ti.rows - tr, kTileM));
+        const int m16 = (rows + 15) & ~15;
+        const int r0 = ti.r0 + tr;
+        const bool full_box = V::kARows == kTileM && p.a_box128 && m16 == kTileM;
+        const int box_pid = V::kPair ? 1 : 0;                    // producer of a single 128-row token box
+        const int nbox = m16 / 16;
+        const int my_a_bytes = full_box ? (pid == box_pid ? kABytes : 0) : ((nbox + 1 - pid) / 2) * 16 * kBlockK;
+        const bool my_b = V::kPair ? pid == 0 : (pid == 0 || ti.n > 128);
         const uint32_t bytes = (uint32_t)((my_b ? V::kWeightBoxTx : 0) + my_a_bytes);
         const CUtensorMap* tm_b = ti.layer == 1 ? &tm_w1 : &tm_w2;
         const CUtensorMap* tm_a = ti.layer == 1 ? (full_box ? &tm_xs128 : &tm_xs16)
                                                 : (full_box ? &tm_l1a128 : &tm_l1a16);
-        const int b_row = ti.layer == 1 ? ti.e * 2 * p.I + ti.nb * kL1Feat + pid * p.I
-                                        : ti.e * p.H + ti.nb * kTileN + pid * 128;
+        const int bsel = V::kPair ? (int)crank : pid;             // which 128-row half of the weight tile
+        const int b_row = ti.layer == 1 ? ti.e * 2 * p.I + ti.nb * kL1Feat + bsel * p.I
+                                        : ti.e * p.H + ti.nb * kTileN + bsel * 128;
         for (int kk0 = 0; kk0 < ti.ks; kk0 += kSub) {
           const int nsub = min(kSub, ti.ks - kk0);
           if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, ctrl, to, (kSiteEmpty << 24) | tag)) { ok = false; break; }
           const uint32_t fb = smem_u32(&full[stage]);
-          mbar_arrive_expect_tx(fb, bytes * (uint32_t)nsub);
+          const uint32_t fbar = V::kPair ? cluster_addr(fb, 0) : fb;
+          if constexpr (V::kPair) mbar_arrive_expect_tx_cluster(fbar, bytes * (uint32_t)nsub);
+          else mbar_arrive_expect_tx(fbar, bytes * (uint32_t)nsub);
           for (int u = 0; u < nsub; ++u) {
             const int gs = stage * kSub + u;
             const uint32_t a_dst = smem_u32(sA + gs * kABytes);
-            const uint32_t b_dst = smem_u32(sB + gs * kBBytes) + (uint32_t)(pid * 128 * kBlockK);
+            const uint32_t b_dst = smem_u32(sB + gs * V::kBStageBytes) + (uint32_t)(V::kPair ? 0 : pid * 128 * kBlockK);
             const int kx = (kk0 + u) * V::kKStage;
-            if (my_b) tma_load_2d(b_dst, tm_b, fb, kx, b_row);
+            auto load = [&](uint32_t dst, const CUtensorMap* m, int y) {
+              if constexpr (V::kPair) tma_load_2d_pair(dst, m, fbar, kx, y);
+              else tma_load_2d(dst, m, fbar, kx, y);
+            };
+            if (my_b) load(b_dst, tm_b, b_row);
             if (full_box) {
-              if (pid == 0) tma_load_2d(a_dst, tm_a, fb, kx, ti.r0);
+              if (pid == box_pid) load(a_dst, tm_a, r0);
             } else {
-              for (int j = pid; j < nbox; j += 2) tma_load_2d(a_dst + j * 16 * kBlockK, tm_a, fb, kx, ti.r0 + 16 * j);
+              for (int j = pid; j < nbox; j += 2) load(a_dst + j * 16 * kBlockK, tm_a, r0 + 16 * j);
             }
           }
           ++issued;
@@ -422,8 +490,8 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
       s_misc[2 + 3 * pid] = issued;     // s_misc[2] (producer 0), s_misc[5] (producer 1)
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------- MMA issuer
+    if (lane == 0 && leader) {
+      // ---------------- MMA issuer (in a pair: the even CTA's, for both)
       // Stage s's descriptors are stage 0's plus s * (stage bytes / 16) in the
       // start-address field (shared addresses stay below 256 KB: no carry).
       const uint64_t a_desc0 = desc_sw128(smem_u32(sA));
@@ -431,6 +499,9 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
       const uint64_t sfa_desc0 = desc_sf(smem_u32(sSFA));
       const uint64_t sfb_desc0 = desc_sf(smem_u32(sSFB));
       const uint32_t full0 = smem_u32(&full[0]), empty0 = smem_u32(&empty[0]);
+      // a pair commits to the odd CTA's barriers as well (same offsets there)
+      const uint32_t empty0_peer = V::kPair ? cluster_addr(empty0, 1) : 0u;
+      const uint32_t tfull_peer = V::kPair ? cluster_addr(smem_u32(tfull), 1) : 0u;
       uint32_t stage = 0, phase = 0, aphase = 0, consumed = 0;
       bool ok = true;
       TileFeed feed(s_tiles, tile_full, tile_empty);
@@ -438,9 +509,9 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
         Tile ti;
         if (!feed.take(ctrl, to, ok, ti)) break;
         const uint32_t tag = (uint32_t)ti.tag;
-        if (!mbar_wait(smem_u32(tempty), aphase ^ 1u, ctrl, to, (kSiteTmemEmpty << 24) | tag)) break;
+        if (!mbar_wait<V::kPair>(smem_u32(tempty), aphase ^ 1u, ctrl, to, (kSiteTmemEmpty << 24) | tag)) break;
         tc_fence_after();
-        const uint32_t id0 = idesc_mx((uint32_t)ti.n, 0u);
+        const uint32_t id0 = idesc_mx((uint32_t)ti.n, 0u, (uint32_t)(kTileM * G));
         const uint32_t id1 = id0 | (1u << 4) | (1u << 29);
         const uint32_t id2 = id0 | (2u << 4) | (2u << 29);
         const uint32_t id3 = id0 | (3u << 4) | (3u << 29);
@@ -448,12 +519,12 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
         const uint32_t idb = idesc_bf16((uint32_t)ti.n);
         for (int kk0 = 0; kk0 < ti.ks; kk0 += kSub) {
           const int nsub = min(kSub, ti.ks - kk0);
-          if (!mbar_wait(full0 + stage * 8u, phase, ctrl, to, (kSiteFull << 24) | tag)) { ok = false; break; }
+          if (!mbar_wait<V::kPair>(full0 + stage * 8u, phase, ctrl, to, (kSiteFull << 24) | tag)) { ok = false; break; }
           for (int u = 0; u < nsub; ++u) {
             const uint32_t so = (uint32_t)(stage * kSub + u);
             const uint32_t acc0 = (kk0 + u) != 0 ? 1u : 0u;
             const uint64_t ad = a_desc0 + (uint64_t)(so * (uint32_t)(kABytes >> 4));
-            const uint64_t bd = b_desc0 + (uint64_t)(so * (uint32_t)(kBBytes >> 4));
+            const uint64_t bd = b_desc0 + (uint64_t)(so * (uint32_t)(V::kBStageBytes >> 4));
             if constexpr (V::kBf16) {
               tc_mma_f16(tmem, ad, bd, idb, acc0);                       // K = 16 each: +32 bytes
               tc_mma_f16(tmem, ad + 2, bd + 2, idb, 1u);
@@ -462,25 +533,27 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
             } else {
               const uint64_t sfb_d = sfb_desc0 + (uint64_t)(so * (uint32_t)(kSFBBytes >> 4));
               const uint32_t sfa_t = tmem + kSFCol0 + so * kSFSetCols, sfb_t = sfa_t + 4;
-              tc_cp_sf(sfa_t, sfa_desc0 + (uint64_t)(so * (uint32_t)(kSFABytes >> 4)));
-              tc_cp_sf(sfb_t, sfb_d);
-              if (two_sfb) tc_cp_sf(sfb_t + 4, sfb_d + (512 >> 4));
-              tc_mma_mx(tmem, ad, bd, id0, sfa_t, sfb_t, acc0);
-              tc_mma_mx_acc(tmem, ad + 2, bd + 2, id1, sfa_t, sfb_t);   // K = 32 each: +32 bytes
-              tc_mma_mx_acc(tmem, ad + 4, bd + 4, id2, sfa_t, sfb_t);
-              tc_mma_mx_acc(tmem, ad + 6, bd + 6, id3, sfa_t, sfb_t);
+              tc_cp_sf<G>(sfa_t, sfa_desc0 + (uint64_t)(so * (uint32_t)(kSFABytes >> 4)));
+              tc_cp_sf<G>(sfb_t, sfb_d);
+              if (two_sfb) tc_cp_sf<G>(sfb_t + 4, sfb_d + (512 >> 4));
+              tc_mma_mx<G>(tmem, ad, bd, id0, sfa_t, sfb_t, acc0);
+              tc_mma_mx_acc<G>(tmem, ad + 2, bd + 2, id1, sfa_t, sfb_t);   // K = 32 each: +32 bytes
+              tc_mma_mx_acc<G>(tmem, ad + 4, bd + 4, id2, sfa_t, sfb_t);
+              tc_mma_mx_acc<G>(tmem, ad + 6, bd + 6, id3, sfa_t, sfb_t);
             }
           }
-          tc_commit(empty0 + stage * 8u);
+          tc_commit<G>(empty0 + stage * 8u);
+          if constexpr (V::kPair) tc_commit<G>(empty0_peer + stage * 8u);
           ++consumed;
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
-        tc_commit(smem_u32(tfull));
+        tc_commit<G>(smem_u32(tfull));
+        if constexpr (V::kPair) tc_commit<G>(tfull_peer);
         aphase ^= 1u;
       }
       s_misc[1] = consumed;
-      tc_commit(smem_u32(drain));
+      tc_commit<G>(smem_u32(drain));
       if (!mbar_wait_drain(smem_u32(drain), 0, to)) set_error(ctrl, MM_ERR_TIMEOUT, kSiteDrain << 24);
     }
   } else if (warp == 2 && V::kBf16) {
@@ -498,11 +571,15 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
     // Then, stage by stage, it writes the stage's bytes into the 32x4x4 atom
     // layout (one 16-byte shared store per atom and lane), every lane fences
     // them (the tensor core reads through the async proxy) and lane 0 arrives
-    // on the stage's full barrier.
+    // on the stage's full barrier.  In a pair each CTA writes the atoms of its
+    // own token rows and both weight atoms (the MMA reads the weight scales of
+    // all 256 rows from each CTA's TMEM), and arrives on the even CTA's barrier.
     uint32_t stage = 0, phase = 0, armed = 0;
     int ready_key = -1;
     const int H32 = p.H / 32, I32 = p.I / 32;
     TileFeed feed(s_tiles, tile_full, tile_empty);
+    if constexpr (V::kPair) feed.pair(crank);
+    const uint32_t full0_cl = V::kPair ? cluster_addr(smem_u32(&full[0]), 0) : 0u;
     for (;;) {
       bool fed = true;
       Tile ti;
@@ -514,7 +591,8 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
         if (lane == 0) {
           ok = (ti.layer == 1)
                    ? counter_wait(&arrival[ti.e], (uint32_t)__ldg(counts + ti.e), ctrl, to, (kSiteArrival << 24) | tag)
-                   : counter_wait(&l1_done[ti.e], l1_tiles_of(items, ti.e, p.mt1), ctrl, to, (kSiteL1Done << 24) | tag);
+                   : counter_wait(&l1_done[ti.e], G * l1_tiles_of(items, ti.e, p.mt1), ctrl, to,
+                                  (kSiteL1Done << 24) | tag);
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
@@ -531,11 +609,14 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
       const bool two_sfb = ti.n > 128;
       const bool a_vec = (kstride & 15) == 0;                                    // workspace rows
       const bool b_vec = a_vec && (reinterpret_cast<uintptr_t>(b_sf_base) & 15) == 0;
+      const int tr = (int)crank * kTileM;                        // this CTA's first row of the block
+      const int m16 = (max(0, min(ti.rows - tr, kTileM)) + 15) & ~15;
+      const int r0 = ti.r0 + tr;
       const uint8_t* a_row[4];
       const uint8_t* b_row[8];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const int slot = min(ti.r0 + lane + 32 * j, p.A - 1);
+        const int slot = min(r0 + lane + 32 * j, p.A - 1);
         a_row[j] = a_sf_base + (size_t)slot * kstride;
         b_row[j] = b_sf_base + (size_t)(b_row0 + lane + 32 * j) * kstride;
         b_row[4 + j] = b_sf_base + (size_t)((two_sfb ? b_row1 : b_row0) + lane + 32 * j) * kstride;
@@ -545,7 +626,7 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
         uint32_t a[4][4], b[8][4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          if (lane + 32 * j < ti.m16) {
+          if (lane + 32 * j < m16) {
             if (a_vec && ng == 4) {
               const uint4 v = __ldcg(reinterpret_cast<const uint4*>(a_row[j] + g0 * 4));
               a[j][0] = v.x; a[j][1] = v.y; a[j][2] = v.z; a[j][3] = v.w;
@@ -590,7 +671,10 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
           }
           fence_proxy_async_shared();
           __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&full[stage]));
+          if (lane == 0) {
+            if constexpr (V::kPair) mbar_arrive_cluster(full0_cl + stage * 8u);
+            else mbar_arrive(smem_u32(&full[stage]));
+          }
           ++armed;
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
@@ -607,11 +691,15 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
     uint32_t aphase = 0;
     int vote_buf = 0;
     TileFeed feed(s_tiles, tile_full, tile_empty);
+    if constexpr (V::kPair) feed.pair(crank);
+    // the accumulator is freed on the MMA-issuing CTA's barrier
+    const uint32_t tempty_bar = V::kPair ? cluster_addr(smem_u32(tempty), 0) : smem_u32(tempty);
     for (;;) {
       bool ok = true;
       Tile ti;
       if (feed.take_warp(lane, ctrl, to, ok, ti)) {
-        if (lane == 0) ok = mbar_wait(smem_u32(tfull), aphase, ctrl, to, (kSiteTmemFull << 24) | (uint32_t)ti.tag);
+        if (lane == 0)
+          ok = mbar_wait<V::kPair>(smem_u32(tfull), aphase, ctrl, to, (kSiteTmemFull << 24) | (uint32_t)ti.tag);
         ok = __shfl_sync(0xffffffffu, ok, 0);
       } else {
         ok = false;      // end of the feed (or abort): leave together
@@ -630,10 +718,12 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
       // L2), frees the accumulator for the next tile's MMAs, and only then does
       // the arithmetic and the stores.
       const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16);
-      const int row = q * 32 + lane;                       // token row of the block
-      const bool valid = row < ti.rows;
-      const size_t slot = (size_t)ti.r0 + row;
-      const bool live_warp = q * 32 < ti.rows;             // warp-uniform: some row of this quarter is live
+      const int tr = (int)crank * kTileM;                  // this CTA's first row of the block
+      const int rows = max(0, min(ti.rows - tr, kTileM));  // this CTA's rows (all of them outside a pair)
+      const int row = q * 32 + lane;                       // token row of this CTA's share
+      const bool valid = row < rows;
+      const size_t slot = (size_t)ti.r0 + tr + row;
+      const bool live_warp = q * 32 < rows;                // warp-uniform: some row of this quarter is live
       float v[128];
       const int nh = ti.layer == 1 ? kL1Feat / 2 : ti.n >> 1;   // this warp's columns (per operand for L1)
       if (live_warp) {
@@ -653,7 +743,10 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(tempty));
+      if (lane == 0) {
+        if constexpr (V::kPair) mbar_arrive_cluster(tempty_bar);
+        else mbar_arrive(tempty_bar);
+      }
       if (live_warp) {
         if (V::kBf16 && ti.layer == 1) {
           // ---- L1 of the bf16 layer: features [64hh, 64hh + 64): clamp + SwiGLU, rounded to bf16
@@ -739,7 +832,7 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
             for (int i = 0; i < 4; ++i) {
               const int r = rr + 8 * i;
               fr[i] = __shfl_sync(0xffffffffu, f, r);
-              live |= (q * 32 + r < ti.rows ? 1u : 0u) << i;
+              live |= (q * 32 + r < rows ? 1u : 0u) << i;
             }
             float* const col0 = stage_out + ti.nb * kTileN + c_beg + 4 * cc;
             const int wsw = (lane >> 1) & 3;
@@ -782,27 +875,47 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
     __threadfence();
   }
 
+  }  // !skip
+
   // ------------------------------------------------------------ teardown
   __syncthreads();
-  if (threadIdx.x == 0) {
+  // A pair: both CTAs' roles have stopped and recorded their counts before the
+  // even CTA drains, and it finishes draining before either CTA frees its TMEM
+  // or exits (loads of both CTAs complete on the even CTA's barriers, and its
+  // MMAs read the odd CTA's shared memory).
+  if constexpr (V::kPair) cluster_sync();
+  if (threadIdx.x == 0 && leader) {
     // After an abort, TMA loads may still be landing.  Each issued but
-    // unconsumed stage's barrier completes once its bytes land, provided the
-    // scale loader's and both producers' arrivals were made; make the missing
-    // ones here (a role that stopped early: its arrival, no bytes; the scale
-    // loader has already waited for its own copies).
-    const uint32_t issued0 = s_misc[2], issued1 = s_misc[5], consumed = s_misc[1], armed = s_misc[4];
-    const uint32_t issued = issued0 > issued1 ? issued0 : issued1;
+    // unconsumed stage's barrier completes once its bytes land, provided every
+    // role's arrival was made; make the missing ones here (a role that stopped
+    // early: its arrival, no bytes; the scale loader has already waited for its
+    // own copies).  Roles: each CTA's two producers and scale loader.
+    uint32_t cnt[3 * G];
+    cnt[0] = s_misc[2];
+    cnt[1] = s_misc[5];
+    cnt[2] = V::kBf16 ? 0xFFFFFFFFu : s_misc[4];
+    if constexpr (V::kPair) {
+      const uint32_t misc_peer = cluster_addr(smem_u32(s_misc), 1);
+      cnt[3] = ld_cluster_u32(misc_peer + 4 * 2);
+      cnt[4] = ld_cluster_u32(misc_peer + 4 * 5);
+      cnt[5] = ld_cluster_u32(misc_peer + 4 * 4);
+    }
+    const uint32_t consumed = s_misc[1];
+    uint32_t issued = 0;
+#pragma unroll
+    for (int c = 0; c < G; ++c) issued = max(issued, max(cnt[3 * c], cnt[3 * c + 1]));
     for (uint32_t s = consumed; s < issued; ++s) {
       const uint32_t bar = smem_u32(&full[s % kStages]);
-      if (!V::kBf16 && s >= armed) mbar_arrive(bar);
-      if (s >= issued0) mbar_arrive(bar);
-      if (s >= issued1) mbar_arrive(bar);
+#pragma unroll
+      for (int r = 0; r < 3 * G; ++r)
+        if (s >= cnt[r]) mbar_arrive(bar);
       if (!mbar_wait_drain(bar, (s / kStages) & 1u, to)) set_error(ctrl, MM_ERR_TIMEOUT, kSiteDrain << 24);
     }
   }
+  if constexpr (V::kPair) cluster_sync();
   if (warp == 1) {
     tc_fence_after();
-    tc_dealloc(tmem, kTmemCols);
+    tc_dealloc<G>(tmem, kTmemCols);
   }
 }
 
@@ -864,29 +977,71 @@ __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ Fo
 // Template kernels are configured and launched in the translation unit that
 // defines them.
 int layer_max_rows(int variant) {
-  return (variant == kVariantThin || variant == kVariantBf16Thin) ? ThinVariant::kARows : WideVariant::kARows;
+  switch (variant) {
+    case kVariantThin: return ThinVariant::kBlockRows;
+    case kVariantBf16Thin: return Bf16ThinVariant::kBlockRows;
+    case kVariantPair: return PairVariant::kBlockRows;
+    default: return WideVariant::kBlockRows;
+  }
 }
 
 template <class V>
-static cudaError_t prepare_one(int* ctas_per_sm) {
-  cudaError_t e = cudaFuncSetAttribute(megamoe_kernel<V>, cudaFuncAttributeMaxDynamicSharedMemorySize, V::kSmemBytes);
-  if (e != cudaSuccess) return e;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, megamoe_kernel<V>, kThreads, V::kSmemBytes);
+static cudaLaunchConfig_t launch_config(int grid, cudaStream_t stream, cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = V::kSmemBytes;
+  cfg.stream = stream;
+  attr->id = cudaLaunchAttributeClusterDimension;
+  attr->val.clusterDim.x = V::kCtas;
+  attr->val.clusterDim.y = 1;
+  attr->val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
 }
 
-cudaError_t layer_prepare(int variant, int* ctas_per_sm) {
+// CTAs of the layer kernel that can be resident at once on the whole device
+// (for a pair: twice the clusters that fit).
+template <class V>
+static cudaError_t prepare_one(int* resident, int sms) {
+  cudaError_t e = cudaFuncSetAttribute(megamoe_kernel<V>, cudaFuncAttributeMaxDynamicSharedMemorySize, V::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  if constexpr (V::kPair) {
+    cudaLaunchAttribute attr;
+    cudaLaunchConfig_t cfg = launch_config<V>(2 * (sms / 2), nullptr, &attr);
+    int clusters = 0;
+    e = cudaOccupancyMaxActiveClusters(&clusters, megamoe_kernel<V>, &cfg);
+    *resident = 2 * clusters;
+    return e;
+  } else {
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, megamoe_kernel<V>, kThreads, V::kSmemBytes);
+    *resident = per_sm * sms;
+    return e;
+  }
+}
+
+cudaError_t layer_prepare(int variant, int sms, int* resident) {
   switch (variant) {
-    case kVariantThin: return prepare_one<ThinVariant>(ctas_per_sm);
-    case kVariantBf16Wide: return prepare_one<Bf16WideVariant>(ctas_per_sm);
-    case kVariantBf16Thin: return prepare_one<Bf16ThinVariant>(ctas_per_sm);
-    default: return prepare_one<WideVariant>(ctas_per_sm);
+    case kVariantThin: return prepare_one<ThinVariant>(resident, sms);
+    case kVariantBf16Wide: return prepare_one<Bf16WideVariant>(resident, sms);
+    case kVariantBf16Thin: return prepare_one<Bf16ThinVariant>(resident, sms);
+    case kVariantPair: return prepare_one<PairVariant>(resident, sms);
+    default: return prepare_one<WideVariant>(resident, sms);
   }
 }
 
 template <class V>
 static cudaError_t launch_one(int grid, cudaStream_t stream, const CUtensorMap* maps, const ForwardParams& p) {
-  megamoe_kernel<V><<<grid, kThreads, V::kSmemBytes, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p);
-  return cudaGetLastError();
+  if constexpr (V::kPair) {
+    cudaLaunchAttribute attr;
+    cudaLaunchConfig_t cfg = launch_config<V>(grid, stream, &attr);
+    return cudaLaunchKernelEx(&cfg, megamoe_kernel<V>, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p);
+  } else {
+    megamoe_kernel<V><<<grid, kThreads, V::kSmemBytes, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p);
+    return cudaGetLastError();
+  }
 }
 
 // maps: W1, W2, dispatched tokens (16- and 128-row boxes), L1 activations (16- and 128-row boxes)
@@ -898,6 +1053,7 @@ cudaError_t layer_launch(int variant, int grid, cudaStream_t stream, const CUten
     case kVariantThin: e = launch_one<ThinVariant>(grid, stream, maps, p); break;
     case kVariantBf16Wide: e = launch_one<Bf16WideVariant>(grid, stream, maps, p); break;
     case kVariantBf16Thin: e = launch_one<Bf16ThinVariant>(grid, stream, maps, p); break;
+    case kVariantPair: e = launch_one<PairVariant>(grid, stream, maps, p); break;
     default: e = launch_one<WideVariant>(grid, stream, maps, p); break;
   }
   if (e != cudaSuccess) return e;

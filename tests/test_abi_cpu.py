@@ -218,3 +218,27 @@ def test_forward_without_device(lib):
     assert _fwd() == mm.MM_ERR_NO_DEVICE
     assert _fwd_bf16() == mm.MM_ERR_NO_DEVICE
     assert _bf16_layer() == mm.MM_ERR_NO_DEVICE
+
+
+def test_layer_variant_choice(lib):
+    """Host-side choice of the layer kernel (no GPU needed): decode-sized
+    batches (at most 16 assignments per expert on average) take the thin
+    stages; larger ones take two-CTA tiles when hidden is a multiple of 256
+    and the pair switch is on, else one-CTA tiles; the bf16 layer never pairs."""
+    import moe_expert_layer_idx_gb300 as mm
+
+    prev = mm.mm_set_pair_mma(1)
+    try:
+        assert mm.mm_layer_variant(128, 256, 8, 7168) == 1          # decode: 4 per expert
+        assert mm.mm_layer_variant(512, 256, 8, 7168) == 1          # exactly 16 per expert
+        assert mm.mm_layer_variant(8192, 256, 8, 7168) == 4         # prefill: pair
+        assert mm.mm_layer_variant(400, 3, 2, 384) == 0             # hidden 384: one-CTA tiles
+        assert mm.mm_layer_variant(8192, 256, 8, 7168, True) == 3 - 1   # bf16 wide
+        assert mm.mm_layer_variant(128, 256, 8, 7168, True) == 3    # bf16 thin
+        assert mm.mm_set_pair_mma(0) == 1
+        assert mm.mm_get_pair_mma() == 0
+        assert mm.mm_layer_variant(8192, 256, 8, 7168) == 0
+        assert mm.mm_layer_variant(0, 8, 2, 256) == 1
+        assert mm.mm_layer_variant(-1, 8, 2, 256) == mm.MM_ERR_INVALID_ARG
+    finally:
+        mm.mm_set_pair_mma(prev)
