@@ -21,9 +21,12 @@ What it computes (the single-GPU fused MegaMoE expert layer):
 * ``moe_bf16`` -- the bf16 x bf16 variant of the layer (the BF16 MegaMoE kernel
   that DeepGEMM PR #451 fixes beside the FP8/FP4 one): the same steps with
   bfloat16 inputs, weights and L1 activations instead of the FP8/FP4 codes.
+* ``moe_f8b``  -- the layer in the (1, 128, 128) recipe (E4M3 activations and
+  weights with fp32 scales per 1 x 128 and 128 x 128 blocks; the SM90 recipe
+  of the DeepGEMM SM90 MegaMoE dev log, Phase 1 entry).
 
 Every function is pinned by CPU tests (``tests/test_oracle_*.py``) against
 closed forms, library routines, brute force and exact rational arithmetic;
 none is "parity unpinned".
 """
-from . import formats, routing, moe, moe_bf16  # noqa: F401
+from . import formats, routing, moe, moe_bf16, moe_f8b  # noqa: F401
