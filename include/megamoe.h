@@ -305,6 +305,48 @@ int mm_quantize_mx(const float* src, long long rows, long long cols, int fmt,
                    void* dst, void* dst_sf, mm_stream_t stream);
 
 /*
+ * mm_quantize_f8b -- the block quantiser of the (1, 128, 128) recipe, the one
+ * the SM90 path of the pages uses with float scale factors ([P3] Phase 1
+ * entry): src float32 [rows, cols] (cols a multiple of 128, rows a multiple
+ * of block_rows, 16-byte aligned) -> E4M3 codes dst [rows, cols] (4-byte
+ * aligned) and one float32 scale per block of block_rows x 128 in dst_sf
+ * [rows / block_rows, cols / 128] (4-byte aligned).  block_rows is 1 (token
+ * activations: one scale per token and 128 elements) or 128 (weights: one
+ * scale per 128 x 128 block).  For a block with largest magnitude a the scale
+ * is s = a / 448 rounded to fp32 (1 for an all-zero block) and each element's
+ * code is the round-to-nearest-even E4M3 value of the fp32 quotient v / s,
+ * saturating.  MM_ERR_INVALID_ARG for bad sizes or pointers.
+ */
+int mm_quantize_f8b(const float* src, long long rows, long long cols, int block_rows, void* dst, float* dst_sf,
+                    mm_stream_t stream);
+
+/*
+ * mm_f8b_forward -- the fused layer in the (1, 128, 128) recipe ([P3] Phase 1
+ * entry: the SM90 wrapper's recipe (1, 128, 128) with float scale factors):
+ *
+ *   x      E4M3 codes   [T, H]              16-byte aligned
+ *   x_sf   float32      [T, H/128]          one scale per token and 128 elements of H
+ *   l1_w   E4M3 codes   [E, 2I, H]          rows [0, I) gate, [I, 2I) up; 32-byte aligned
+ *   l1_sf  float32      [E, 2I/128, H/128]  one scale per 128 x 128 block
+ *   l2_w   E4M3 codes   [E, H, I]           32-byte aligned
+ *   l2_sf  float32      [E, H/128, I/128]
+ *   (scale arrays 4-byte aligned; the values as mm_quantize_f8b makes them)
+ *
+ * a1 = sum over the 128-wide K blocks b of (x_sf[t, b] * l1_sf[e, n/128, b])
+ * * (E4M3 dot product of block b), accumulated in fp32; then the clamp and
+ * SwiGLU of mm_forward; the L1 activations are requantised by the rule of
+ * mm_quantize_f8b with one scale per token and 128 features; L2 likewise with
+ * l2_sf; y = bf16(sum over j ascending of topk_w * o), as mm_forward.
+ * topk_idx, topk_w, y, clamp, num_sms, the workspace (mm_workspace_size bytes)
+ * and stream, and the error behaviour (mm_get_status) are those of mm_forward.
+ */
+int mm_f8b_forward(int num_tokens, int experts, int topk, int hidden, int inter,
+                   const void* x, const float* x_sf, const int32_t* topk_idx, const float* topk_w,
+                   const void* l1_w, const float* l1_sf, const void* l2_w, const float* l2_sf,
+                   void* y, float clamp, int num_sms,
+                   void* workspace, size_t workspace_bytes, mm_stream_t stream);
+
+/*
  * mm_forward_noalloc -- mm_forward without a caller-provided workspace.  The
  * pages have no counterpart to this entry point.
  *

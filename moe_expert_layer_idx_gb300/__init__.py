@@ -57,6 +57,8 @@ _SIGS = {
     "mm_forward_bf16": (_c_int, [_c_int] * 5 + [_c_vp] * 8 + [ctypes.c_float, _c_int, _c_vp, _c_size, _c_vp]),
     "mm_bf16_workspace_size": (_c_size, [_c_int] * 5),
     "mm_bf16_forward": (_c_int, [_c_int] * 5 + [_c_vp] * 6 + [ctypes.c_float, _c_int, _c_vp, _c_size, _c_vp]),
+    "mm_f8b_forward": (_c_int, [_c_int] * 5 + [_c_vp] * 9 + [ctypes.c_float, _c_int, _c_vp, _c_size, _c_vp]),
+    "mm_quantize_f8b": (_c_int, [_c_vp, _c_ll, _c_ll, _c_int, _c_vp, _c_vp, _c_vp]),
 }
 
 
@@ -135,6 +137,22 @@ def mm_bf16_forward(num_tokens, experts, topk, hidden, inter, x, topk_idx, topk_
     return lib().mm_bf16_forward(num_tokens, experts, topk, hidden, inter, _ptr(x), _ptr(topk_idx), _ptr(topk_w),
                                  _ptr(l1_w), _ptr(l2_w), _ptr(y), float(clamp), num_sms, _ptr(workspace),
                                  workspace_bytes, _stream(stream))
+
+
+def mm_f8b_forward(num_tokens, experts, topk, hidden, inter, x, x_sf, topk_idx, topk_w, l1_w, l1_sf, l2_w,
+                   l2_sf, y, clamp, num_sms, workspace, workspace_bytes=None, stream=None) -> int:
+    """The layer in the (1, 128, 128) recipe: E4M3 activations and weights with
+    float32 scales per 1 x 128 (x_sf) and 128 x 128 (l1_sf, l2_sf) blocks."""
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    return lib().mm_f8b_forward(num_tokens, experts, topk, hidden, inter, _ptr(x), _ptr(x_sf), _ptr(topk_idx),
+                                _ptr(topk_w), _ptr(l1_w), _ptr(l1_sf), _ptr(l2_w), _ptr(l2_sf), _ptr(y),
+                                float(clamp), num_sms, _ptr(workspace), workspace_bytes, _stream(stream))
+
+
+def mm_quantize_f8b(src, rows, cols, block_rows, dst, dst_sf, stream=None) -> int:
+    """fp32 [rows, cols] -> E4M3 codes + float32 scales per block_rows x 128 block."""
+    return lib().mm_quantize_f8b(_ptr(src), rows, cols, block_rows, _ptr(dst), _ptr(dst_sf), _stream(stream))
 
 
 def mm_set_reserved_sms(n) -> int:

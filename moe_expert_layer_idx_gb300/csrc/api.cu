@@ -19,6 +19,8 @@ cudaError_t layer_prepare(int variant, int sms, int* resident);
 cudaError_t layer_launch(int variant, int grid, cudaStream_t stream, const CUtensorMap* maps, const ForwardParams& p);
 cudaError_t launch_quantize(const float* src, long long nblocks, bool e4m3, uint8_t* dst, uint8_t* sf,
                             int grid, cudaStream_t stream);
+cudaError_t launch_quantize_f8b(const float* src, long long rows, long long cols, int block_rows, uint8_t* dst,
+                                float* sf, int max_ctas, cudaStream_t stream);
 }  // namespace mm
 
 using namespace mm;
@@ -237,12 +239,15 @@ int mm_grid_size(int device_sms, int reserved_sms, int num_sms, int max_resident
 void mm_set_wait_timeout_ns(unsigned long long ns) { g_timeout_ns.store(ns ? ns : kDefaultTimeoutNs); }
 unsigned long long mm_get_wait_timeout_ns(void) { return g_timeout_ns.load(); }
 
-// The fused layer.  FP8 x FP4 layer (bf16_layer false): E4M3 activations
+// The fused layer.  recipe kMx (FP8 x FP4, UE8M0 per 32): E4M3 activations
 // (x, x_sf) when x_bf16 is null, else bf16 activations quantised in the
-// dispatch.  bf16 x bf16 layer (bf16_layer true): bf16 activations in x and
-// bf16 weights, no scale factors.  A missing input is MM_ERR_INVALID_ARG
-// (after the shape checks and the T = 0 early return).
-static int forward_impl(bool bf16_layer, int num_tokens, int experts, int topk, int hidden, int inter,
+// dispatch.  kBf16 (bf16 x bf16): bf16 activations in x and bf16 weights, no
+// scale factors.  kF8B (the (1, 128, 128) recipe): E4M3 activations and
+// weights, fp32 scales per 1 x 128 (x_sf) and 128 x 128 (l1_sf, l2_sf) blocks.
+// A missing input is MM_ERR_INVALID_ARG (after the shape checks and the T = 0
+// early return).
+enum Recipe : int { kMx = 0, kBf16 = 1, kF8B = 2 };
+static int forward_impl(int recipe, int num_tokens, int experts, int topk, int hidden, int inter,
                         const void* x, const void* x_sf, const void* x_bf16, const int32_t* topk_idx,
                         const float* topk_w, const void* l1_w, const void* l1_sf, const void* l2_w,
                         const void* l2_sf, void* y, float clamp, int num_sms,
@@ -251,6 +256,7 @@ static int forward_impl(bool bf16_layer, int num_tokens, int experts, int topk, 
   int rc = check_shape(T, E, k, H, I);
   if (rc != MM_OK) return rc;
   if (T == 0) return MM_OK;
+  const bool bf16_layer = recipe == kBf16, f8b = recipe == kF8B;
   const bool fp8_in = !bf16_layer && x_bf16 == nullptr;
   const bool scales = !bf16_layer;
   if ((bf16_layer && !x) || (fp8_in && (!x || !x_sf)) || !topk_idx || !topk_w || !l1_w || !l2_w || !y ||
@@ -270,7 +276,7 @@ static int forward_impl(bool bf16_layer, int num_tokens, int experts, int topk, 
   DevState* st;
   rc = device_state(&dev, &st);
   if (rc != MM_OK) return rc;
-  const int variant = pick_variant((long long)T * k, E, H, bf16_layer);
+  const int variant = f8b ? (int)kVariantF8B : pick_variant((long long)T * k, E, H, bf16_layer);
   const int grid = mm_grid_size(st->sms, reserved_now(), num_sms, st->max_resident[variant]);
   const int A = T * k;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -289,6 +295,16 @@ static int forward_impl(bool bf16_layer, int num_tokens, int experts, int topk, 
         encode_2d(&maps[3], bf, ws + L.xs, (uint64_t)H, (uint64_t)A, (uint64_t)H * 2, kk, kTileM) != MM_OK ||
         encode_2d(&maps[4], bf, ws + L.l1a, (uint64_t)I, (uint64_t)A, (uint64_t)I * 2, kk, 16) != MM_OK ||
         encode_2d(&maps[5], bf, ws + L.l1a, (uint64_t)I, (uint64_t)A, (uint64_t)I * 2, kk, kTileM) != MM_OK)
+      return MM_ERR_CUDA;
+  } else if (f8b) {
+    // E4M3 weights [rows][K], one byte per element, 128 x 128 boxes
+    const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    if (encode_2d(&maps[0], u8, l1_w, (uint64_t)H, (uint64_t)E * 2 * I, H, kBlockK, 128) != MM_OK ||
+        encode_2d(&maps[1], u8, l2_w, (uint64_t)I, (uint64_t)E * H, I, kBlockK, 128) != MM_OK ||
+        encode_2d(&maps[2], u8, ws + L.xs, (uint64_t)H, (uint64_t)A, H, kBlockK, 16) != MM_OK ||
+        encode_2d(&maps[3], u8, ws + L.xs, (uint64_t)H, (uint64_t)A, H, kBlockK, kTileM) != MM_OK ||
+        encode_2d(&maps[4], u8, ws + L.l1a, (uint64_t)I, (uint64_t)A, I, kBlockK, 16) != MM_OK ||
+        encode_2d(&maps[5], u8, ws + L.l1a, (uint64_t)I, (uint64_t)A, I, kBlockK, kTileM) != MM_OK)
       return MM_ERR_CUDA;
   } else if (encode_2d(&maps[0], CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, l1_w, (uint64_t)H, (uint64_t)E * 2 * I, H / 2,
                 kBlockK, 128) != MM_OK ||
@@ -333,7 +349,17 @@ int mm_forward(int num_tokens, int experts, int topk, int hidden, int inter,
                const void* l1_w, const void* l1_sf, const void* l2_w, const void* l2_sf,
                void* y, float clamp, int num_sms,
                void* workspace, size_t workspace_bytes, mm_stream_t stream) {
-  return forward_impl(false, num_tokens, experts, topk, hidden, inter, x, x_sf, nullptr, topk_idx, topk_w, l1_w,
+  return forward_impl(kMx, num_tokens, experts, topk, hidden, inter, x, x_sf, nullptr, topk_idx, topk_w, l1_w,
+                      l1_sf, l2_w, l2_sf, y, clamp, num_sms, workspace, workspace_bytes, stream);
+}
+
+int mm_f8b_forward(int num_tokens, int experts, int topk, int hidden, int inter,
+                   const void* x, const float* x_sf, const int32_t* topk_idx, const float* topk_w,
+                   const void* l1_w, const float* l1_sf, const void* l2_w, const float* l2_sf,
+                   void* y, float clamp, int num_sms,
+                   void* workspace, size_t workspace_bytes, mm_stream_t stream) {
+  if ((l1_w && !aligned(l1_w, 16)) || (l2_w && !aligned(l2_w, 16))) return MM_ERR_INVALID_ARG;
+  return forward_impl(kF8B, num_tokens, experts, topk, hidden, inter, x, x_sf, nullptr, topk_idx, topk_w, l1_w,
                       l1_sf, l2_w, l2_sf, y, clamp, num_sms, workspace, workspace_bytes, stream);
 }
 
@@ -342,7 +368,7 @@ int mm_forward_bf16(int num_tokens, int experts, int topk, int hidden, int inter
                     const void* l1_w, const void* l1_sf, const void* l2_w, const void* l2_sf,
                     void* y, float clamp, int num_sms,
                     void* workspace, size_t workspace_bytes, mm_stream_t stream) {
-  return forward_impl(false, num_tokens, experts, topk, hidden, inter, nullptr, nullptr, x_bf16, topk_idx, topk_w,
+  return forward_impl(kMx, num_tokens, experts, topk, hidden, inter, nullptr, nullptr, x_bf16, topk_idx, topk_w,
                       l1_w, l1_sf, l2_w, l2_sf, y, clamp, num_sms, workspace, workspace_bytes, stream);
 }
 
@@ -355,7 +381,7 @@ int mm_bf16_forward(int num_tokens, int experts, int topk, int hidden, int inter
                     const void* x, const int32_t* topk_idx, const float* topk_w,
                     const void* l1_w, const void* l2_w, void* y, float clamp, int num_sms,
                     void* workspace, size_t workspace_bytes, mm_stream_t stream) {
-  return forward_impl(true, num_tokens, experts, topk, hidden, inter, x, nullptr, nullptr, topk_idx, topk_w, l1_w,
+  return forward_impl(kBf16, num_tokens, experts, topk, hidden, inter, x, nullptr, nullptr, topk_idx, topk_w, l1_w,
                       nullptr, l2_w, nullptr, y, clamp, num_sms, workspace, workspace_bytes, stream);
 }
 
@@ -439,3 +465,21 @@ int mm_quantize_mx(const float* src, long long rows, long long cols, int fmt, vo
 }
 
 }  // extern "C"
+
+extern "C" int mm_quantize_f8b(const float* src, long long rows, long long cols, int block_rows, void* dst,
+                               float* dst_sf, mm_stream_t stream) {
+  if (rows < 0 || cols < 0 || cols % 128 != 0) return MM_ERR_INVALID_ARG;
+  if (block_rows != 1 && block_rows != 128) return MM_ERR_INVALID_ARG;
+  if (rows % block_rows != 0) return MM_ERR_INVALID_ARG;
+  if (block_rows == 128 && (rows > (1ll << 31) - 1 || cols > (1ll << 31) - 1)) return MM_ERR_INVALID_ARG;
+  if (rows * cols == 0) return MM_OK;
+  if (!src || !dst || !dst_sf || !aligned(src, 16) || !aligned(dst, 4) || !aligned(dst_sf, 4)) return MM_ERR_INVALID_ARG;
+  int dev;
+  DevState* st;
+  int rc = device_state(&dev, &st);
+  if (rc != MM_OK) return rc;
+  if (launch_quantize_f8b(src, rows, cols, block_rows, static_cast<uint8_t*>(dst), dst_sf, st->sms * 16,
+                          reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return MM_ERR_CUDA;
+  return MM_OK;
+}

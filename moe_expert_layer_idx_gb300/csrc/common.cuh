@@ -69,7 +69,15 @@ constexpr uint32_t kSFSetCols = 12;                 // SFA: +0..3, SFB: +4..11
 // instead of once per 128.  The even CTA of the pair issues every MMA; the
 // odd one loads its share, writes its scale atoms and runs the epilogue of
 // its 128 accumulator rows.
-template <int kARows_, int kStages_, bool kXpose_, bool kBf16_, int kSub_ = 1, bool kPair_ = false>
+//
+// kF8B: the (1, 128, 128) recipe: E4M3 activations and weights with fp32
+// scales per 1 x 128 and 128 x 128 blocks.  The MMA (kind::f8f6f4, no block
+// scales) writes each 128-wide K stage into one of two partial accumulators
+// in TMEM; the epilogue warps add partial x (token scale x weight-block scale)
+// into fp32 registers, stage by stage, and requantise the L1 activations with
+// one fp32 scale per token and 128 features.
+template <int kARows_, int kStages_, bool kXpose_, bool kBf16_, int kSub_ = 1, bool kPair_ = false,
+          bool kF8B_ = false>
 struct Variant {
   static constexpr int kARows = kARows_;
   static constexpr int kStages = kStages_;            // ring slots
@@ -79,10 +87,13 @@ struct Variant {
   static constexpr bool kBf16 = kBf16_;
   static constexpr bool kPair = kPair_;
   static_assert(!kPair || (!kBf16 && kARows == kTileM && kSub == 1), "the pair variant is the wide FP8 x FP4 one");
+  static constexpr bool kF8B = kF8B_;
+  static_assert(!kF8B || (!kBf16 && !kPair && kARows == kTileM && kSub == 1), "the per-128 recipe runs wide tiles");
+  static constexpr bool kNoSF = kBf16 || kF8B;         // no block-scale atoms for the MMA
   static constexpr int kCtas = kPair ? 2 : 1;          // CTAs that share one MMA tile
   static constexpr int kBlockRows = kARows * kCtas;    // largest token block of a tile
   static constexpr int kKStage = kBf16 ? kBlockK / 2 : kBlockK;     // K elements per stage
-  static constexpr int kWeightBoxTx = kBf16 ? 128 * 128 : kBHalfTxBytes;   // one 128-row weight box
+  static constexpr int kWeightBoxTx = kNoSF ? 128 * 128 : kBHalfTxBytes;   // one 128-row weight box (bytes)
   static constexpr int kABytes = kARows * kBlockK;
   static constexpr int kBStageBytes = kPair ? kBBytes / 2 : kBBytes;       // weight rows this CTA holds
   static constexpr int kStageBytes = kABytes + kBStageBytes + kSFABytes + kSFBBytes;
@@ -90,12 +101,15 @@ struct Variant {
   // L2 epilogue stores whole 64-byte row segments instead of 16-byte pieces of
   // 32 different rows.
   static constexpr int kXposeBytes = kXpose ? kEpiWarps * 32 * 16 * 4 : 0;
-  static constexpr int kSmemBytes = kStages * kSub * kStageBytes + kXposeBytes + kBarBytes + 1024 /*align*/;
+  // kF8B: per-row block maxima exchanged by the two warps of a lane quarter
+  static constexpr int kAmaxBytes = kF8B ? kEpiWarps * 32 * 4 : 0;
+  static constexpr int kSmemBytes = kStages * kSub * kStageBytes + kXposeBytes + kAmaxBytes + kBarBytes + 1024 /*align*/;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
   static_assert(kABytes % 1024 == 0 && kBStageBytes % 1024 == 0, "SW128 tiles need 1 KB alignment");
   static_assert(kARows % 16 == 0 && kARows <= kTileM, "token rows per stage");
-  // barriers (2 per stage, 3 accumulator/drain, 2 per tile-ring slot), misc words, votes, tile ring
-  static_assert((2 * kStages + 3 + 2 * kTileRing) * 8 + 8 * 4 + 2 * kEpiWarps * 4 + kTileRing * 9 * 4 <= kBarBytes,
+  // barriers (2 per stage, 3 accumulator/drain, 2 per tile-ring slot, 4 partial-accumulator),
+  // misc words, votes, tile ring
+  static_assert((2 * kStages + 3 + 2 * kTileRing + 4) * 8 + 8 * 4 + 2 * kEpiWarps * 4 + kTileRing * 9 * 4 <= kBarBytes,
                 "barrier region");
   static_assert(kSFCol0 + kStages * kSub * kSFSetCols <= kTmemCols, "scale-factor sets fit TMEM");
   // the MMA's 128-row A window of the last sub-stage stays inside the allocation
@@ -106,8 +120,10 @@ using ThinVariant = Variant<32, 3, false, false, 2>;
 using Bf16WideVariant = Variant<128, 4, true, true>;
 using Bf16ThinVariant = Variant<32, 6, false, true>;
 using PairVariant = Variant<128, 6, true, false, 1, true>;
+using F8BVariant = Variant<128, 4, true, false, 1, false, true>;
 enum VariantId : int {
-  kVariantWide = 0, kVariantThin = 1, kVariantBf16Wide = 2, kVariantBf16Thin = 3, kVariantPair = 4, kNumVariants = 5
+  kVariantWide = 0, kVariantThin = 1, kVariantBf16Wide = 2, kVariantBf16Thin = 3, kVariantPair = 4, kVariantF8B = 5,
+  kNumVariants = 6
 };
 
 
@@ -543,6 +559,27 @@ __device__ __forceinline__ uint32_t idesc_bf16(uint32_t n) {
   d |= (n >> 3) << 17;             // N / 8
   d |= (128u >> 4) << 24;          // M / 16
   return d;
+}
+// Instruction descriptor of kind::f8f6f4 without block scales: A = E4M3 tokens
+// (M = 128), B = E4M3 weights (N), fp32 accumulator, both K-major.
+__device__ __forceinline__ uint32_t idesc_f8(uint32_t n) {
+  uint32_t d = 0;
+  d |= 1u << 4;                    // accumulator format: F32
+  d |= 0u << 7;                    // A format: E4M3
+  d |= 0u << 10;                   // B format: E4M3
+  d |= (n >> 3) << 17;             // N / 8
+  d |= (128u >> 4) << 24;          // M / 16
+  return d;
+}
+// D (+)= A . B^T, E4M3 operands (K = 32 per instruction), no scales.
+__device__ __forceinline__ void tc_mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
+      :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
 }
 // D (+)= A . B^T, bf16 operands (K = 16 per instruction).
 __device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,

@@ -221,7 +221,8 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
   uint8_t* sSFA = sB + kSubs * V::kBStageBytes;       // [kSubs] token scale atom
   uint8_t* sSFB = sSFA + kSubs * kSFABytes;           // [kSubs] two weight scale atoms
   float* sX = reinterpret_cast<float*>(sSFB + kSubs * kSFBBytes);   // [kEpiWarps] transpose buffers
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sSFB + kSubs * kSFBBytes + V::kXposeBytes);
+  float* sAmax = reinterpret_cast<float*>(sSFB + kSubs * kSFBBytes + V::kXposeBytes);   // kF8B: [4][2][32]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sSFB + kSubs * kSFBBytes + V::kXposeBytes + V::kAmaxBytes);
   uint64_t* full = bars;                     // [kStages] both producers' TMA bytes + the scale loader's atoms
   uint64_t* empty = bars + kStages;          // [kStages] MMAs reading the stage are done
   uint64_t* tfull = bars + 2 * kStages;      // accumulator ready
@@ -229,9 +230,11 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
   uint64_t* drain = tempty + 1;              // final MMA drain
   uint64_t* tile_full = drain + 1;           // [kTileRing] tile index published
   uint64_t* tile_empty = tile_full + kTileRing;   // [kTileRing] read by every consumer role
+  uint64_t* pfull = tile_empty + kTileRing;       // kF8B: [2] partial accumulator written
+  uint64_t* pempty = pfull + 2;                   // kF8B: [2] partial accumulator taken by every epilogue warp
   // tmem base, stages consumed (MMA), stages issued (producer 0), status read at the start, stages
   // armed (scale loader), stages issued (producer 1)
-  uint32_t* s_misc = reinterpret_cast<uint32_t*>(tile_empty + kTileRing);
+  uint32_t* s_misc = reinterpret_cast<uint32_t*>(pempty + 2);
   int32_t* s_vote = reinterpret_cast<int32_t*>(s_misc + 8);    // epilogue votes [2][kEpiWarps]
   Tile* s_tiles = reinterpret_cast<Tile*>(s_vote + 2 * kEpiWarps);   // [kTileRing] claimed tiles
 
@@ -265,7 +268,7 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       // producers (+ the scale loader), of both CTAs of a pair
-      mbar_init(&full[s], (V::kBf16 ? 2 : 2 + 1) * G);
+      mbar_init(&full[s], (V::kNoSF ? 2 : 2 + 1) * G);
       mbar_init(&empty[s], 1);
     }
     mbar_init(tfull, 1);
@@ -274,6 +277,10 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
     for (int i = 0; i < kTileRing; ++i) {
       mbar_init(&tile_full[i], 1);
       mbar_init(&tile_empty[i], kTileReaders * G);   // a pair's odd CTA has as many readers as the even one
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&pfull[i], 1);
+      mbar_init(&pempty[i], kEpiWarps);
     }
     for (int i = 1; i < 8; ++i) s_misc[i] = 0;
     s_misc[3] = status0;                        // read by the odd CTA of a pair
@@ -503,20 +510,24 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
       const uint32_t empty0_peer = V::kPair ? cluster_addr(empty0, 1) : 0u;
       const uint32_t tfull_peer = V::kPair ? cluster_addr(smem_u32(tfull), 1) : 0u;
       uint32_t stage = 0, phase = 0, aphase = 0, consumed = 0;
+      uint32_t pc = 0;                               // kF8B: partial accumulators written
       bool ok = true;
       TileFeed feed(s_tiles, tile_full, tile_empty);
       while (ok) {
         Tile ti;
         if (!feed.take(ctrl, to, ok, ti)) break;
         const uint32_t tag = (uint32_t)ti.tag;
-        if (!mbar_wait<V::kPair>(smem_u32(tempty), aphase ^ 1u, ctrl, to, (kSiteTmemEmpty << 24) | tag)) break;
-        tc_fence_after();
+        if constexpr (!V::kF8B) {
+          if (!mbar_wait<V::kPair>(smem_u32(tempty), aphase ^ 1u, ctrl, to, (kSiteTmemEmpty << 24) | tag)) break;
+          tc_fence_after();
+        }
         const uint32_t id0 = idesc_mx((uint32_t)ti.n, 0u, (uint32_t)(kTileM * G));
         const uint32_t id1 = id0 | (1u << 4) | (1u << 29);
         const uint32_t id2 = id0 | (2u << 4) | (2u << 29);
         const uint32_t id3 = id0 | (3u << 4) | (3u << 29);
         const bool two_sfb = ti.n > 128;
         const uint32_t idb = idesc_bf16((uint32_t)ti.n);
+        const uint32_t idf8 = idesc_f8((uint32_t)ti.n);
         for (int kk0 = 0; kk0 < ti.ks; kk0 += kSub) {
           const int nsub = min(kSub, ti.ks - kk0);
           if (!mbar_wait<V::kPair>(full0 + stage * 8u, phase, ctrl, to, (kSiteFull << 24) | tag)) { ok = false; break; }
@@ -525,7 +536,20 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
             const uint32_t acc0 = (kk0 + u) != 0 ? 1u : 0u;
             const uint64_t ad = a_desc0 + (uint64_t)(so * (uint32_t)(kABytes >> 4));
             const uint64_t bd = b_desc0 + (uint64_t)(so * (uint32_t)(V::kBStageBytes >> 4));
-            if constexpr (V::kBf16) {
+            if constexpr (V::kF8B) {
+              // each 128-K stage into its own partial accumulator (alternating halves of TMEM),
+              // once the epilogue has taken that half's previous partial
+              const uint32_t pb = pc & 1u, pph = (pc >> 1) & 1u;
+              if (!mbar_wait(smem_u32(&pempty[pb]), pph ^ 1u, ctrl, to, (kSiteTmemEmpty << 24) | tag)) { ok = false; break; }
+              tc_fence_after();
+              const uint32_t d = tmem + 256u * pb;
+              tc_mma_f8(d, ad, bd, idf8, 0u);                            // K = 32 each: +32 bytes
+              tc_mma_f8(d, ad + 2, bd + 2, idf8, 1u);
+              tc_mma_f8(d, ad + 4, bd + 4, idf8, 1u);
+              tc_mma_f8(d, ad + 6, bd + 6, idf8, 1u);
+              tc_commit<G>(smem_u32(&pfull[pb]));
+              ++pc;
+            } else if constexpr (V::kBf16) {
               tc_mma_f16(tmem, ad, bd, idb, acc0);                       // K = 16 each: +32 bytes
               tc_mma_f16(tmem, ad + 2, bd + 2, idb, 1u);
               tc_mma_f16(tmem, ad + 4, bd + 4, idb, 1u);
@@ -548,15 +572,17 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
-        tc_commit<G>(smem_u32(tfull));
-        if constexpr (V::kPair) tc_commit<G>(tfull_peer);
+        if constexpr (!V::kF8B) {
+          tc_commit<G>(smem_u32(tfull));
+          if constexpr (V::kPair) tc_commit<G>(tfull_peer);
+        }
         aphase ^= 1u;
       }
       s_misc[1] = consumed;
       tc_commit<G>(smem_u32(drain));
       if (!mbar_wait_drain(smem_u32(drain), 0, to)) set_error(ctrl, MM_ERR_TIMEOUT, kSiteDrain << 24);
     }
-  } else if (warp == 2 && V::kBf16) {
+  } else if (warp == 2 && V::kNoSF) {
     // ---------------- no scale factors in the bf16 layer: only follow the tile feed
     TileFeed feed(s_tiles, tile_full, tile_empty);
     bool fed = true;
@@ -694,16 +720,21 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
     if constexpr (V::kPair) feed.pair(crank);
     // the accumulator is freed on the MMA-issuing CTA's barrier
     const uint32_t tempty_bar = V::kPair ? cluster_addr(smem_u32(tempty), 0) : smem_u32(tempty);
+    uint32_t pc = 0;                 // kF8B: partial accumulators taken
+    bool failed = false;             // kF8B: a wait inside the last tile gave up
     for (;;) {
       bool ok = true;
       Tile ti;
       if (feed.take_warp(lane, ctrl, to, ok, ti)) {
-        if (lane == 0)
-          ok = mbar_wait<V::kPair>(smem_u32(tfull), aphase, ctrl, to, (kSiteTmemFull << 24) | (uint32_t)ti.tag);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if constexpr (!V::kF8B) {
+          if (lane == 0)
+            ok = mbar_wait<V::kPair>(smem_u32(tfull), aphase, ctrl, to, (kSiteTmemFull << 24) | (uint32_t)ti.tag);
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+        }
       } else {
         ok = false;      // end of the feed (or abort): leave together
       }
+      ok = ok && !failed;
       // the epilogue warps decide together, so none waits alone on a named barrier
       if (lane == 0) s_vote[vote_buf * kEpiWarps + ew] = ok ? 1 : 0;
       named_bar_sync(3, 32 * kEpiWarps);
@@ -726,7 +757,55 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
       const bool live_warp = q * 32 < rows;                // warp-uniform: some row of this quarter is live
       float v[128];
       const int nh = ti.layer == 1 ? kL1Feat / 2 : ti.n >> 1;   // this warp's columns (per operand for L1)
-      if (live_warp) {
+      if constexpr (V::kF8B) {
+        // ---- the (1, 128, 128) recipe: v += partial(kk) x (token scale x weight-block scale), stage by stage
+#pragma unroll
+        for (int i = 0; i < 128; ++i) v[i] = 0.f;
+        // the token scales were written by other CTAs (dispatch, or the L1 epilogue): acquire their release
+        if (ti.layer == 1) (void)ld_acquire(&arrival[ti.e]); else (void)ld_acquire(&l1_done[ti.e]);
+        const int kb = ti.ks;                                        // 128-wide K blocks per row
+        const float* tok_s = reinterpret_cast<const float*>(ti.layer == 1 ? xs_sf : l1a_sf) +
+                             (size_t)min((int)slot, p.A - 1) * kb;
+        const float* w_s = reinterpret_cast<const float*>(ti.layer == 1 ? p.w1_sf : p.w2_sf);
+        // weight-scale rows: L1 the gate block nb and the up block I/128 + nb of expert e; L2 the
+        // 128-row block that holds this warp's output columns
+        const size_t wr0 = ti.layer == 1 ? ((size_t)ti.e * (2 * p.I / 128) + ti.nb) * kb
+                                         : ((size_t)ti.e * (p.H / 128) + (ti.nb * kTileN + hh * nh) / 128) * kb;
+        const size_t wr1 = ti.layer == 1 ? wr0 + (size_t)(p.I / 128) * kb : wr0;
+        for (int kk = 0; kk < kb; ++kk) {
+          const uint32_t pb = pc & 1u, pph = (pc >> 1) & 1u;
+          ++pc;
+          bool got = true;
+          if (lane == 0) got = mbar_wait(smem_u32(&pfull[pb]), pph, ctrl, to, (kSiteTmemFull << 24) | (uint32_t)ti.tag);
+          got = __shfl_sync(0xffffffffu, got, 0);
+          if (got) {
+            tc_fence_after();
+            if (live_warp) {
+              const float sx = valid ? __ldcg(tok_s + kk) : 0.f;
+              const float c0 = sx * __ldg(w_s + wr0 + kk), c1 = sx * __ldg(w_s + wr1 + kk);
+              const uint32_t pbase = tbase + 256u * pb;
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const bool l1 = ti.layer == 1;
+                if (!l1 && j * 16 >= nh) break;
+                const uint32_t col = l1 ? (uint32_t)((j < 4 ? 0 : kL1Feat) + hh * 64 + (j & 3) * 16)
+                                        : (uint32_t)(hh * nh + j * 16);
+                float t16[16];
+                tc_ld16(pbase + col, t16);
+                tc_wait_ld();
+                const float c = (l1 && j >= 4) ? c1 : c0;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) v[j * 16 + i] = fmaf(t16[i], c, v[j * 16 + i]);
+              }
+            }
+          } else {
+            failed = true;
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&pempty[pb]));
+        }
+      } else if (live_warp) {
         if (ti.layer == 1) {
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
@@ -741,13 +820,50 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
         }
         tc_wait_ld();
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        if constexpr (V::kPair) mbar_arrive_cluster(tempty_bar);
-        else mbar_arrive(tempty_bar);
+      if constexpr (!V::kF8B) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if constexpr (V::kPair) mbar_arrive_cluster(tempty_bar);
+          else mbar_arrive(tempty_bar);
+        }
       }
-      if (live_warp) {
+      if (V::kF8B && ti.layer == 1) {
+        // ---- L1 of the (1, 128, 128) recipe (every epilogue warp: the block max is exchanged
+        // through shared memory with the partner warp that holds the other 64 features of the
+        // token's 128): clamp + SwiGLU in fp32, one fp32 scale per 128 features, E4M3 codes
+        const float L = p.clamp;
+        float a = 0.f;
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          float gg = v[i], uu = v[64 + i];
+          if (p.use_clamp) {
+            gg = fminf(gg, L);
+            uu = fminf(fmaxf(uu, -L), L);
+          }
+          v[i] = gg * __fdividef(1.0f, 1.0f + __expf(-gg)) * uu;   // fast-math SiLU
+          a = fmaxf(a, fabsf(v[i]));
+        }
+        sAmax[(q * 2 + hh) * 32 + lane] = a;
+        named_bar_sync(4, 32 * kEpiWarps);
+        a = fmaxf(a, sAmax[(q * 2 + (hh ^ 1)) * 32 + lane]);
+        const float sc = a == 0.f ? 1.0f : __fdiv_rn(a, 448.0f);
+        if (valid) {
+          uint4* d4 = reinterpret_cast<uint4*>(l1a + slot * p.I + ti.nb * kL1Feat + hh * 64);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            uint32_t w[4];
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+              const float* hv = &v[16 * i + 4 * b];
+              w[b] = e4m3_code(__fdiv_rn(hv[0], sc)) | (e4m3_code(__fdiv_rn(hv[1], sc)) << 8) |
+                     (e4m3_code(__fdiv_rn(hv[2], sc)) << 16) | (e4m3_code(__fdiv_rn(hv[3], sc)) << 24);
+            }
+            d4[i] = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+          if (hh == 0) reinterpret_cast<float*>(l1a_sf)[slot * (p.I / 128) + ti.nb] = sc;
+        }
+      } else if (live_warp) {
         if (V::kBf16 && ti.layer == 1) {
           // ---- L1 of the bf16 layer: features [64hh, 64hh + 64): clamp + SwiGLU, rounded to bf16
           const float L = p.clamp;
@@ -893,7 +1009,7 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
     uint32_t cnt[3 * G];
     cnt[0] = s_misc[2];
     cnt[1] = s_misc[5];
-    cnt[2] = V::kBf16 ? 0xFFFFFFFFu : s_misc[4];
+    cnt[2] = V::kNoSF ? 0xFFFFFFFFu : s_misc[4];
     if constexpr (V::kPair) {
       const uint32_t misc_peer = cluster_addr(smem_u32(s_misc), 1);
       cnt[3] = ld_cluster_u32(misc_peer + 4 * 2);
@@ -981,6 +1097,7 @@ int layer_max_rows(int variant) {
     case kVariantThin: return ThinVariant::kBlockRows;
     case kVariantBf16Thin: return Bf16ThinVariant::kBlockRows;
     case kVariantPair: return PairVariant::kBlockRows;
+    case kVariantF8B: return F8BVariant::kBlockRows;
     default: return WideVariant::kBlockRows;
   }
 }
@@ -1028,6 +1145,7 @@ cudaError_t layer_prepare(int variant, int sms, int* resident) {
     case kVariantBf16Wide: return prepare_one<Bf16WideVariant>(resident, sms);
     case kVariantBf16Thin: return prepare_one<Bf16ThinVariant>(resident, sms);
     case kVariantPair: return prepare_one<PairVariant>(resident, sms);
+    case kVariantF8B: return prepare_one<F8BVariant>(resident, sms);
     default: return prepare_one<WideVariant>(resident, sms);
   }
 }
@@ -1054,6 +1172,7 @@ cudaError_t layer_launch(int variant, int grid, cudaStream_t stream, const CUten
     case kVariantBf16Wide: e = launch_one<Bf16WideVariant>(grid, stream, maps, p); break;
     case kVariantBf16Thin: e = launch_one<Bf16ThinVariant>(grid, stream, maps, p); break;
     case kVariantPair: e = launch_one<PairVariant>(grid, stream, maps, p); break;
+    case kVariantF8B: e = launch_one<F8BVariant>(grid, stream, maps, p); break;
     default: e = launch_one<WideVariant>(grid, stream, maps, p); break;
   }
   if (e != cudaSuccess) return e;
