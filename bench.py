@@ -227,10 +227,21 @@ def _quant(mm, src, rows, cols, fmt, out, out_sf):
         raise RuntimeError(f"mm_quantize_mx: {mm.STATUS_NAMES.get(rc, rc)}")
 
 
-def _make_weights(mm, synth, torch, cfg, dev, bf16_layer):
+def _quant_f8b(mm, src, rows, cols, block_rows, out, out_sf):
+    rc = mm.mm_quantize_f8b(src, rows, cols, block_rows, out, out_sf)
+    if rc != mm.MM_OK:
+        raise RuntimeError(f"mm_quantize_f8b: {mm.STATUS_NAMES.get(rc, rc)}")
+
+
+def _make_weights(mm, synth, torch, cfg, dev, bf16_layer, f8b=False):
     """Seeded expert weights, quantised on the device by the library's own kernel."""
     E, H, I = cfg.E, cfg.H, cfg.I
-    if bf16_layer:
+    if f8b:
+        l1_w = torch.empty(E, 2 * I, H, dtype=torch.uint8, device=dev)
+        l1_sf = torch.empty(E, 2 * I // 128, H // 128, dtype=torch.float32, device=dev)
+        l2_w = torch.empty(E, H, I, dtype=torch.uint8, device=dev)
+        l2_sf = torch.empty(E, H // 128, I // 128, dtype=torch.float32, device=dev)
+    elif bf16_layer:
         l1_w = torch.empty(E, 2 * I, H, dtype=torch.bfloat16, device=dev)
         l2_w = torch.empty(E, H, I, dtype=torch.bfloat16, device=dev)
         l1_sf = l2_sf = None
@@ -245,12 +256,16 @@ def _make_weights(mm, synth, torch, cfg, dev, bf16_layer):
         e1 = min(E, e0 + chunk)
         n1, n2 = (e1 - e0) * 2 * I * H, (e1 - e0) * H * I
         synth.normal_f32_cuda(cfg.seed, synth.TENSOR_W1, e0 * 2 * I * H, buf[:n1], synth.weight_scale(H))
-        if bf16_layer:
+        if f8b:
+            _quant_f8b(mm, buf[:n1], (e1 - e0) * 2 * I, H, 128, l1_w[e0:e1], l1_sf[e0:e1])
+        elif bf16_layer:
             l1_w[e0:e1].copy_(buf[:n1].view(e1 - e0, 2 * I, H))
         else:
             _quant(mm, buf[:n1], (e1 - e0) * 2 * I, H, mm.MM_FMT_E2M1, l1_w[e0:e1], l1_sf[e0:e1])
         synth.normal_f32_cuda(cfg.seed, synth.TENSOR_W2, e0 * H * I, buf[:n2], synth.weight_scale(I))
-        if bf16_layer:
+        if f8b:
+            _quant_f8b(mm, buf[:n2], (e1 - e0) * H, I, 128, l2_w[e0:e1], l2_sf[e0:e1])
+        elif bf16_layer:
             l2_w[e0:e1].copy_(buf[:n2].view(e1 - e0, H, I))
         else:
             _quant(mm, buf[:n2], (e1 - e0) * H, I, mm.MM_FMT_E2M1, l2_w[e0:e1], l2_sf[e0:e1])
@@ -258,11 +273,15 @@ def _make_weights(mm, synth, torch, cfg, dev, bf16_layer):
     return l1_w, l1_sf, l2_w, l2_sf
 
 
-def _make_tokens(mm, synth, torch, cfg, seed, dev, bf16_layer):
+def _make_tokens(mm, synth, torch, cfg, seed, dev, bf16_layer, f8b=False):
     T, H = cfg.T, cfg.H
     xf = torch.empty(T * H, dtype=torch.float32, device=dev)
     synth.normal_f32_cuda(seed, synth.TENSOR_X, 0, xf)
-    if bf16_layer:
+    if f8b:
+        x = torch.empty(T, H, dtype=torch.uint8, device=dev)
+        x_sf = torch.empty(T, H // 128, dtype=torch.float32, device=dev)
+        _quant_f8b(mm, xf, T, H, 1, x, x_sf)
+    elif bf16_layer:
         x, x_sf = xf.view(T, H).to(torch.bfloat16), None
     else:
         x = torch.empty(T, H, dtype=torch.uint8, device=dev)
@@ -273,7 +292,7 @@ def _make_tokens(mm, synth, torch, cfg, seed, dev, bf16_layer):
     return x, x_sf, torch.from_numpy(idx_np).to(dev), torch.from_numpy(w_np).to(dev), idx_np
 
 
-def _roofline(cfg, ms, idx_np, bf16_layer, workload, kernel, route_ms=None):
+def _roofline(cfg, ms, idx_np, bf16_layer, workload, kernel, route_ms=None, f8b=False):
     """Roofline of one whole step (routing, layer kernel, combine): algorithmic
     bytes (touched experts' weights + scales, x, x_sf, top-k, y) or FLOPs over
     the step time, against the measured peak of the bound that is slower."""
@@ -284,6 +303,9 @@ def _roofline(cfg, ms, idx_np, bf16_layer, workload, kernel, route_ms=None):
     touched = int((counts > 0).sum())
     if bf16_layer:      # bf16 weights (no scales), bf16 x
         alg_bytes = touched * (3 * H * I * 2) + T * H * 2 + T * k * 8 + T * H * 2
+    elif f8b:           # E4M3 weights + fp32 scales per 128 x 128, E4M3 x + fp32 scales per 128
+        alg_bytes = touched * (3 * H * I + 3 * (H // 128) * (I // 128) * 4) + T * H + T * (H // 128) * 4 + \
+            T * k * 8 + T * H * 2
     else:
         alg_bytes = touched * cfg.expert_bytes() + T * H + T * H // 32 + T * k * 8 + T * H * 2
     hbm, bf16, peak_src = _peaks()
@@ -332,10 +354,11 @@ def run_ours(args, rank, world, local_rank):
     seed = cfg.seed + rank                             # replicas: distinct tokens per rank
     T, H, I, E, k = cfg.T, cfg.H, cfg.I, cfg.E, cfg.k
     bf16_layer = args.layer == "bf16"
+    f8b = args.layer == "f8b"
 
     # ---- inputs (synthetic, generated and quantised on the device)
-    l1_w, l1_sf, l2_w, l2_sf = _make_weights(mm, synth, torch, cfg, dev, bf16_layer)
-    x, x_sf, topk_idx, topk_w, idx_np = _make_tokens(mm, synth, torch, cfg, seed, dev, bf16_layer)
+    l1_w, l1_sf, l2_w, l2_sf = _make_weights(mm, synth, torch, cfg, dev, bf16_layer, f8b)
+    x, x_sf, topk_idx, topk_w, idx_np = _make_tokens(mm, synth, torch, cfg, seed, dev, bf16_layer, f8b)
     y = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
     ws_bytes = (mm.mm_bf16_workspace_size if bf16_layer else mm.mm_workspace_size)(T, E, k, H, I)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
@@ -346,6 +369,9 @@ def run_ours(args, rank, world, local_rank):
         if bf16_layer:
             rc = mm.mm_bf16_forward(T, E, k, H, I, x, topk_idx, topk_w, l1_w, l2_w, y, cfg.clamp, 0, ws, ws_bytes,
                                     stream)
+        elif f8b:
+            rc = mm.mm_f8b_forward(T, E, k, H, I, x, x_sf, topk_idx, topk_w, l1_w, l1_sf, l2_w, l2_sf, y, cfg.clamp,
+                                   0, ws, ws_bytes, stream)
         else:
             rc = mm.mm_forward(T, E, k, H, I, x, x_sf, topk_idx, topk_w, l1_w, l1_sf, l2_w, l2_sf, y, cfg.clamp, 0,
                                ws, ws_bytes, stream)
@@ -442,17 +468,19 @@ def run_ours(args, rank, world, local_rank):
     e1_.synchronize()
     check_status()
     e2e_tps, e2e_ms = replica_throughput(e0_.elapsed_time(e1_) / e_steps, T, world, max_over_ranks)
-    h2d = hx.numel() * hx.element_size() + (hsf.numel() if hsf is not None else 0) + hidx.numel() * 4 + hw.numel() * 4
+    h2d = hx.numel() * hx.element_size() + (hsf.numel() * hsf.element_size() if hsf is not None else 0) + \
+        hidx.numel() * 4 + hw.numel() * 4
     d2h = hy.numel() * 2
 
     roofline = _roofline(cfg, ms, idx_np, bf16_layer, args.workload,
-                         "whole step: routing + megamoe_kernel + combine_kernel", route_ms)
-    roofline["layer_kernel"] = mm.VARIANT_NAMES.get(mm.mm_layer_variant(T, E, k, H, bf16_layer))
+                         "whole step: routing + megamoe_kernel + combine_kernel", route_ms, f8b)
+    roofline["layer_kernel"] = ("f8b (one CTA, 128-token tiles, promotion per 128-K stage)" if f8b else
+                                mm.VARIANT_NAMES.get(mm.mm_layer_variant(T, E, k, H, bf16_layer)))
     launches_per_step = (1 if T * k <= 2048 else 3) + 2
 
     # ---- the other full-size configurations, timed the same way (1 GPU only)
     per_config = {}
-    if world == 1 and not bf16_layer and args.per_config:
+    if world == 1 and args.layer == "fp8" and args.per_config:
         del hx, hsf, hidx, hw, hy, ws
         weights = (l1_w, l1_sf, l2_w, l2_sf)
         for name in args.per_config:
@@ -544,13 +572,18 @@ def _oracle_sample(workload, sample_tokens, layer="fp8"):
     from oracle import formats as OF
     from oracle import moe as OM
     from oracle import moe_bf16 as OMB
+    from oracle import moe_f8b as OM8
 
     cfg = synth.CONFIGS[workload]
     idx, w, _ = synth.routing(cfg)
     toks = list(range(min(max(1, sample_tokens), cfg.T)))
     experts = sorted({int(e) for e in idx[toks].reshape(-1) if e >= 0})
     tp = time.perf_counter()
-    if layer == "bf16":
+    if layer == "f8b":
+        xc, xsf = OM8.quantize_tokens_f8b(synth.x_f32(cfg, rows=toks))
+        cache = {e: OM8.quantize_expert_f8b(synth.w1_f32(cfg, e), synth.w2_f32(cfg, e)) for e in experts}
+        run = lambda: OM8.moe_forward_f8b(xc, xsf, idx[toks], w[toks], lambda e: cache[e], cfg.clamp, cfg.E)  # noqa: E731
+    elif layer == "bf16":
         xb = OF.bf16_round(synth.x_f32(cfg, rows=toks))
         cache = {e: (OF.bf16_round(synth.w1_f32(cfg, e)), OF.bf16_round(synth.w2_f32(cfg, e))) for e in experts}
         run = lambda: OMB.moe_forward_bf16(xb, idx[toks], w[toks], lambda e: cache[e], cfg.clamp, cfg.E)  # noqa: E731
@@ -606,8 +639,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode")
-    ap.add_argument("--layer", choices=["fp8", "bf16"], default="fp8",
-                    help="fp8: E4M3 x E2M1 (the default); bf16: the bf16 x bf16 layer")
+    ap.add_argument("--layer", choices=["fp8", "bf16", "f8b"], default="fp8",
+                    help="fp8: E4M3 x E2M1 with UE8M0/32 (the default); bf16: the bf16 x bf16 layer; "
+                         "f8b: the (1, 128, 128) recipe (E4M3 x E4M3, fp32 scales per 1x128 / 128x128)")
     ap.add_argument("--cpu-sample-tokens", type=int, default=8)
     ap.add_argument("--ref-sample-tokens", type=int, default=1,
                     help="tokens per step of the reference arm (the oracle)")
@@ -641,7 +675,7 @@ def main():
         args.per_config = []
     config = {"workload": f"{cfg.name}: {cfg.T} tokens, hidden {cfg.H}, inter {cfg.I}, {cfg.E} experts, "
                           f"top-{cfg.k}, "
-                          f"{'bf16 x bf16' if args.layer == 'bf16' else 'E4M3 x E2M1 with UE8M0/32'}, "
+                          f"{ {'bf16': 'bf16 x bf16', 'f8b': 'E4M3 x E4M3 with fp32 scales per 1x128 / 128x128'}.get(args.layer, 'E4M3 x E2M1 with UE8M0/32')}, "
                           f"clamp {cfg.clamp if cfg.clamp else 'none'}",
               "tokens": cfg.T, "hidden": cfg.H, "inter": cfg.I, "experts": cfg.E, "topk": cfg.k,
               "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
@@ -679,7 +713,7 @@ def main():
     line = {"metric": METRIC, "value": round(res["tokens_per_s"], 1), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(res["ms"], 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16xbf16->f32" if args.layer == "bf16" else "e4m3xe2m1->f32",
+            "dtype": {"bf16": "bf16xbf16->f32", "f8b": "e4m3xe4m3->f32"}.get(args.layer, "e4m3xe2m1->f32"),
             "data": "synthetic", "config": config, "roofline": res["roofline"], "cpu_baseline": cpu,
             "e2e": res["e2e"], "gpu_launches": res["gpu_launches"], "clocks": res["clocks"],
             "route_ms": round(res["route_ms"], 4), "step_ms_percentiles": res["step_ms"]}
