@@ -284,6 +284,9 @@ int mm_read_routing(int num_tokens, int experts, int topk, int hidden, int inter
  *     indexed by the flat assignment t*k+j
  *  13 routing chunk table: int32 [E][C] then [C], C = 1 up to 2048
  *     assignments, else min(ceil(T*k / 1024), 128) chunks
+ *  14 token blocks, in block order: int32 {expert, the expert's first
+ *     block, its first slot, its count} per block (room for T*k blocks;
+ *     region 3 entry E is the number used)
  * Returns MM_OK, or MM_ERR_INVALID_ARG for an unknown region or shape.
  */
 int mm_workspace_region(int which, int num_tokens, int experts, int topk, int hidden,

@@ -31,7 +31,8 @@ MM_FMT_E4M3 = 0
 MM_FMT_E2M1 = 1
 
 REGIONS = {"ctrl": 0, "counts": 1, "offsets": 2, "items": 3, "arrival": 4, "l1_done": 5, "perm": 6,
-           "inv": 7, "xs": 8, "xs_sf": 9, "l1_acts": 10, "l1_acts_sf": 11, "stage": 12, "route_chunks": 13}
+           "inv": 7, "xs": 8, "xs_sf": 9, "l1_acts": 10, "l1_acts_sf": 11, "stage": 12, "route_chunks": 13,
+           "token_blocks": 14}
 
 _lib = None
 _c_int, _c_size, _c_vp, _c_ll = ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_longlong

@@ -329,6 +329,7 @@ static int forward_impl(int recipe, int num_tokens, int experts, int topk, int h
   fp.use_clamp = (std::isfinite(clamp) && clamp > 0.f) ? 1 : 0;
   fp.clamp = fp.use_clamp ? clamp : 0.f;
   fp.a_box128 = A >= kTileM ? 1 : 0;
+  fp.max_rows = layer_max_rows(variant);
   fp.timeout_ns = g_timeout_ns.load();
   fp.x = (fp8_in || bf16_layer) ? static_cast<const uint8_t*>(x) : nullptr;
   fp.x_sf = fp8_in ? static_cast<const uint8_t*>(x_sf) : nullptr;
@@ -430,15 +431,15 @@ int mm_workspace_region(int which, int num_tokens, int experts, int topk, int hi
                         size_t* offset, size_t* bytes) {
   if (check_shape(num_tokens, experts, topk, hidden, inter) != MM_OK) return MM_ERR_INVALID_ARG;
   const Layout L = make_layout(num_tokens, experts, topk, hidden, inter);
-  const size_t starts[14] = {L.ctrl, L.counts, L.offsets, L.items, L.arrival, L.l1_done, L.perm, L.inv,
-                             L.xs, L.xs_sf, L.l1a, L.l1a_sf, L.stage, L.rhist};
-  if (which < 0 || which > 13) return MM_ERR_INVALID_ARG;
+  const size_t starts[15] = {L.ctrl, L.counts, L.offsets, L.items, L.arrival, L.l1_done, L.perm, L.inv,
+                             L.xs, L.xs_sf, L.l1a, L.l1a_sf, L.stage, L.rhist, L.blocks};
+  if (which < 0 || which > 14) return MM_ERR_INVALID_ARG;
   const size_t A = (size_t)num_tokens * topk;
   const size_t C = (size_t)route_ctas((long long)A);
-  const size_t exact[14] = {4 * (size_t)kCtrlWords, 4 * (size_t)experts, 4 * (size_t)(experts + 1),
+  const size_t exact[15] = {4 * (size_t)kCtrlWords, 4 * (size_t)experts, 4 * (size_t)(experts + 1),
                             4 * (size_t)(experts + 1), 4 * (size_t)experts, 4 * (size_t)experts, 4 * A, 4 * A,
                             A * hidden, A * (hidden / 32), A * inter, A * (inter / 32), A * hidden * 4,
-                            4 * (size_t)experts * C + 4 * C};
+                            4 * (size_t)experts * C + 4 * C, 16 * A};
   if (offset) *offset = starts[which];
   if (bytes) *bytes = exact[which];
   return MM_OK;

@@ -144,7 +144,7 @@ enum WaitSite : uint32_t {
 // ----------------------------------------------------------------- workspace
 struct Layout {
   size_t ctrl, counts, offsets, items, arrival, l1_done, perm, inv;
-  size_t xs, xs_sf, l1a, l1a_sf, stage, rhist, total;
+  size_t xs, xs_sf, l1a, l1a_sf, stage, rhist, blocks, total;
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -183,6 +183,9 @@ __host__ __device__ inline Layout make_layout(long long T, int E, int k, int H, 
   // per-chunk expert counts, then base slots, [E][C] int32, and one bad-index word per chunk
   const size_t C = (size_t)route_ctas((long long)A);
   L.rhist = o;    o = align256(o + 4 * (size_t)E * C + 4 * C);
+  // one record per token block, in block order (at most one block per assignment):
+  // int32 {expert, expert's first block, expert's first slot, expert's count}
+  L.blocks = o;   o = align256(o + 16 * A);
   L.total = o;
   return L;
 }
@@ -200,6 +203,7 @@ struct ForwardParams {
   int use_clamp;
   float clamp;
   int a_box128;                // token count allows one 128-row TMA box per stage
+  int max_rows;                // rows per token block at most (the routing's block size)
   unsigned long long timeout_ns;
   const uint8_t* x;            // E4M3 activations and scales, or
   const uint8_t* x_sf;

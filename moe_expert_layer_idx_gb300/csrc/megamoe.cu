@@ -71,29 +71,24 @@ struct Tile {
 // Tiles are numbered L1 first, then L2; within a layer expert-major, then the
 // weight block, then the token block, so the token blocks that share a weight
 // tile run close together and find it in L2.
-__device__ __forceinline__ void decode_tile(int t, int nL1, const ForwardParams& p, const int32_t* items,
-                                            const int32_t* counts, const int32_t* offsets, Tile& ti) {
+__device__ __forceinline__ void decode_tile(int t, int nL1, const ForwardParams& p, Tile& ti) {
   const bool l1 = t < nL1;
   const int tt = l1 ? t : t - nL1;
   const int NB = l1 ? p.mt1 : p.mt2;
-  int lo = 0, hi = p.E;   // largest e with items[e] * NB <= tt
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (__ldg(items + mid) * NB <= tt) lo = mid; else hi = mid;
-  }
-  const int e = lo;
-  const int i0 = __ldg(items + e);
-  const int mbk = __ldg(items + e + 1) - i0;    // token blocks of this expert
+  // An expert's tiles are [items[e] * NB, items[e + 1] * NB), so tt / NB is
+  // one of its token blocks, whose record names the expert and its tables.
+  const int4 rec = __ldg(reinterpret_cast<const int4*>(p.ws + p.L.blocks) + tt / NB);
+  const int e = rec.x, i0 = rec.y, cnt = rec.w;
+  const int mbk = n_blocks(cnt, p.max_rows);    // token blocks of this expert
   const int local = tt - i0 * NB;
   const int nb = local / mbk;
   const int mb = local - nb * mbk;
-  const int cnt = __ldg(counts + e);
   const int rpb = (cnt + mbk - 1) / mbk;
   const int start = mb * rpb;
   ti.layer = l1 ? 1 : 2;
   ti.e = e;
   ti.nb = nb;
-  ti.r0 = __ldg(offsets + e) + start;
+  ti.r0 = rec.z + start;
   ti.rows = min(rpb, cnt - start);
   ti.m16 = (ti.rows + 15) & ~15;
   ti.n = l1 ? kTileN : min(kTileN, p.H - nb * kTileN);
@@ -147,14 +142,13 @@ struct TileFeed {
   }
 
   // Producer 0: claim, decode, publish.  Returns false at the end of the stream or on abort (ok = false).
-  __device__ bool claim(uint32_t* counter, int total, int nL1, const ForwardParams& p, const int32_t* items,
-                        const int32_t* counts, const int32_t* offsets, uint32_t* ctrl, unsigned long long to,
-                        bool& ok, Tile& ti) {
+  __device__ bool claim(uint32_t* counter, int total, int nL1, const ForwardParams& p, uint32_t* ctrl,
+                        unsigned long long to, bool& ok, Tile& ti) {
     const uint32_t slot = i % kTileRing, ph = (i / kTileRing) & 1u;
     ++i;
     if (!mbar_wait<true>(smem_u32(&empty[slot]), ph ^ 1u, ctrl, to, kSiteTileRing << 24)) { ok = false; return false; }
     const int t = ahead >= 0 ? ahead : (int)atomicAdd(counter, 1u);
-    if (t < total) decode_tile(t, nL1, p, items, counts, offsets, ti);
+    if (t < total) decode_tile(t, nL1, p, ti);
     else ti.layer = 0;
     ring[slot] = ti;
     if (peer_ring_cl != 0) {
@@ -436,7 +430,7 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
       const bool claimer = pid == 0 && leader;
       while (ok) {
         Tile ti;
-        const bool more = claimer ? feed.claim(&ctrl[kNextTile], total, nL1, p, items, counts, offsets, ctrl, to, ok, ti)
+        const bool more = claimer ? feed.claim(&ctrl[kNextTile], total, nL1, p, ctrl, to, ok, ti)
                                   : feed.take(ctrl, to, ok, ti);
         if (!more) break;
         const uint32_t tag = (uint32_t)ti.tag;

@@ -134,12 +134,16 @@ __device__ __forceinline__ void report_bad_index(const RouteParams& p, int first
   ctrl[kAbort] = 1u;
 }
 
-// Counts, offsets and the token-block table from the per-expert totals
-// (thread e < E holds expert e's count).  Returns expert tid's offset.
+// Counts, offsets and the token-block tables from the per-expert totals
+// (thread e < E holds expert e's count): items[e] = the first token block of
+// expert e, and blocks[b] = {e, items[e], offsets[e], counts[e]} for every
+// block b of expert e, so that the layer kernel decodes a tile with one
+// 16-byte load.  Returns expert tid's offset.
 __device__ __forceinline__ int write_tables(const RouteParams& p, int cnt, int* s_warp) {
   int32_t* counts = reinterpret_cast<int32_t*>(p.ws + p.L.counts);
   int32_t* offsets = reinterpret_cast<int32_t*>(p.ws + p.L.offsets);
   int32_t* items = reinterpret_cast<int32_t*>(p.ws + p.L.items);
+  int4* blocks = reinterpret_cast<int4*>(p.ws + p.L.blocks);
   const int tid = threadIdx.x, E = p.E;
   const int off = block_exclusive_scan_1024(cnt, s_warp);
   const int nb = n_blocks(cnt, p.max_n);
@@ -148,6 +152,7 @@ __device__ __forceinline__ int write_tables(const RouteParams& p, int cnt, int* 
     counts[tid] = cnt;
     offsets[tid] = off;
     items[tid] = nb_off;
+    for (int b = 0; b < nb; ++b) blocks[nb_off + b] = make_int4(tid, nb_off, off, cnt);
     if (tid == E - 1) {
       offsets[E] = off + cnt;
       items[E] = nb_off + nb;

@@ -73,3 +73,48 @@ def test_bad_index_is_reported_across_chunks():
     st, *_ = _gpu_route(idx, 16)
     assert st[0] == mm.MM_ERR_BAD_INDEX
     assert st[2] == 400 * 8 + 5
+
+
+# token rows per block of each layer variant (mm_layer_variant's numbering)
+BLOCK_ROWS = {0: 128, 1: 32, 2: 128, 3: 32, 4: 256}
+
+
+def _region(ws, name, T, E, k, H, I, count):
+    off, nb = mm.mm_workspace_region(name, T, E, k, H, I)
+    assert count * 4 <= nb
+    return ws[off:off + 4 * count].view(torch.int32).cpu().numpy()
+
+
+@pytest.mark.parametrize("T,E,k,pair", [(128, 256, 8, False), (8192, 256, 8, False), (4096, 256, 8, False),
+                                        (3001, 37, 7, False), (40, 8, 4, False), (2048, 64, 8, True),
+                                        (700, 5, 3, True)])
+def test_token_block_tables(T, E, k, pair):
+    """items[e] = the first token block of expert e (prefix sum of
+    ceil(count / block rows)), and token block b of expert e carries the
+    record {e, items[e], offsets[e], counts[e]}: both exact, for thin, wide
+    and two-CTA blocks."""
+    H, I = 512, 256
+    rng = np.random.default_rng(T * 7 + E)
+    idx = rng.integers(0, E, (T, k)).astype(np.int32)
+    idx[rng.random((T, k)) < 0.05] = -1
+    prev = mm.mm_get_pair_mma()
+    mm.mm_set_pair_mma(1 if pair else 0)
+    try:
+        variant = mm.mm_layer_variant(T, E, k, H)
+        assert variant == (4 if pair else (1 if T * k <= 16 * E else 0))
+        ws = torch.empty(mm.mm_workspace_size(T, E, k, H, I), dtype=torch.uint8, device="cuda")
+        d_idx = torch.from_numpy(idx).cuda()
+        assert mm.mm_route(T, E, k, H, I, d_idx, ws) == mm.MM_OK
+        torch.cuda.synchronize()
+    finally:
+        mm.mm_set_pair_mma(prev)
+    counts, offsets, _, _ = route(idx, E)
+    nb = (counts + BLOCK_ROWS[variant] - 1) // BLOCK_ROWS[variant]
+    want_items = np.concatenate([[0], np.cumsum(nb)]).astype(np.int32)
+    items = _region(ws, "items", T, E, k, H, I, E + 1)
+    assert np.array_equal(items, want_items)
+    n = int(want_items[-1])
+    rec = _region(ws, "token_blocks", T, E, k, H, I, 4 * n).reshape(n, 4)
+    e = np.repeat(np.arange(E), nb)
+    want = np.stack([e, want_items[e], offsets[e], counts[e]], axis=1).astype(np.int32)
+    assert np.array_equal(rec, want)
