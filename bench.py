@@ -270,6 +270,10 @@ def _make_weights(mm, synth, torch, cfg, dev, bf16_layer, f8b=False):
         else:
             _quant(mm, buf[:n2], (e1 - e0) * H, I, mm.MM_FMT_E2M1, l2_w[e0:e1], l2_sf[e0:e1])
     del buf
+    if not (f8b or bf16_layer):
+        # the one-time transform of the block scales into the layout the layer reads
+        l1_sf = mm.prepare_weight_scales(l1_sf, H)
+        l2_sf = mm.prepare_weight_scales(l2_sf, I)
     return l1_w, l1_sf, l2_w, l2_sf
 
 

@@ -101,9 +101,11 @@ size_t mm_workspace_size(int max_tokens, int experts, int topk, int hidden, int 
  *   l1_w      E2M1, two per byte    [E, 2I, H/2]  element 2c in the low nibble;
  *             rows [0, I) are the gate projection, rows [I, 2I) the up
  *             projection; 32-byte aligned
- *   l1_sf     UE8M0 bytes           [E, 2I, H/32] 4-byte aligned
+ *   l1_sf     UE8M0 scales of l1_w  [E, 2I, H/32] as prepared by
+ *             mm_prepare_weight_scales (rows E*2I, K = H); 16-byte aligned
  *   l2_w      E2M1, two per byte    [E, H, I/2]   32-byte aligned
- *   l2_sf     UE8M0 bytes           [E, H, I/32]  4-byte aligned
+ *   l2_sf     UE8M0 scales of l2_w  [E, H, I/32]  as prepared by
+ *             mm_prepare_weight_scales (rows E*H, K = I); 16-byte aligned
  *   y         bfloat16              [T, H]        16-byte aligned; fully written
  *             (a token whose slots are all empty gets a zero row)
  *   clamp     swiglu limit L: applies iff finite and > 0; then
@@ -279,18 +281,43 @@ int mm_read_routing(int num_tokens, int experts, int topk, int hidden, int inter
  * workspace for the given shape, so tests can inspect intermediates:
  *   0 control block   1 counts      2 offsets     3 work items  4 arrivals
  *   5 L1-done counts  6 perm        7 inv         8 dispatched x [T*k, H]
- *   9 dispatched x_sf [T*k, H/32]  10 l1_acts [T*k, I] (E4M3, slot order)
- *  11 l1_acts_sf [T*k, I/32]        12 weighted L2 outputs, fp32 [T*k, H]
+ *   9 dispatched x scales           10 l1_acts [T*k, I] (E4M3, slot order)
+ *  11 l1_acts scales                12 weighted L2 outputs, fp32 [T*k, H]
  *     indexed by the flat assignment t*k+j
  *  13 routing chunk table: int32 [E][C] then [C], C = 1 up to 2048
  *     assignments, else min(ceil(T*k / 1024), 128) chunks
  *  14 token blocks, in block order: int32 {expert, the expert's first
  *     block, its first slot, its count} per block (room for T*k blocks;
  *     region 3 entry E is the number used)
+ * Regions 9 and 11 hold, for the UE8M0 layers, 512-byte scale atoms (the
+ * layout of mm_prepare_weight_scales) per token block, 128-row half of the
+ * block (two halves for the two-CTA tiles, else one) and 128-wide K stage:
+ * atom ((b * halves + h) * K/128 + s); row r of the half at byte
+ * 16 (r % 32) + 4 (r / 32).  Blocks are those of region 14.  For
+ * mm_f8b_forward they hold fp32 scales [T*k, K/128] in slot order.
  * Returns MM_OK, or MM_ERR_INVALID_ARG for an unknown region or shape.
  */
 int mm_workspace_region(int which, int num_tokens, int experts, int topk, int hidden,
                         int inter, size_t* offset, size_t* bytes);
+
+/*
+ * mm_prepare_weight_scales -- the one-time transform of a weight matrix's
+ * block scales into the layout the layer kernel copies straight into tensor
+ * memory (the pages' SM90 work checks such a weight transform in its Phase 1
+ * smoke test: DeepGEMM fork, "SM90 MegaMoE 开发日志", Phase 1 entry).
+ *   sf    UE8M0 bytes [rows, K/32], row-major (what mm_quantize_mx writes
+ *         for an E2M1 matrix [rows, K]); 4-byte aligned
+ *   out   rows * K/32 bytes, 16-byte aligned, caller-owned: 512-byte atoms
+ *         [rows/128][K/128]; atom (b, s) holds, at byte 16 l + 4 c + j, the
+ *         scale of row 128 b + 32 c + l, block 4 s + j (l < 32, c, j < 4)
+ *   rows  a multiple of 128; K a multiple of 128
+ * The transform is a permutation of bytes: no value changes.  Prepare l1_sf
+ * with rows = E*2I, K = H and l2_sf with rows = E*H, K = I once, when the
+ * weights are loaded; mm_forward, mm_forward_bf16 and mm_forward_noalloc take
+ * the prepared bytes.  Enqueued on `stream`; MM_ERR_INVALID_ARG for bad sizes
+ * or alignment.
+ */
+int mm_prepare_weight_scales(const void* sf, long long rows, long long k, void* out, mm_stream_t stream);
 
 /*
  * mm_quantize_mx -- block quantiser: src float32 [rows, cols] (cols a

@@ -53,6 +53,7 @@ _SIGS = {
     "mm_read_routing": (_c_int, [_c_int] * 5 + [_c_vp] * 5),
     "mm_workspace_region": (_c_int, [_c_int] * 6 + [_c_vp, _c_vp]),
     "mm_quantize_mx": (_c_int, [_c_vp, _c_ll, _c_ll, _c_int, _c_vp, _c_vp, _c_vp]),
+    "mm_prepare_weight_scales": (_c_int, [_c_vp, _c_ll, _c_ll, _c_vp, _c_vp]),
     "mm_forward_noalloc": (_c_int, [_c_int] * 5 + [_c_vp] * 9 + [ctypes.c_float, _c_int, _c_vp]),
     "mm_noalloc_get_status": (_c_int, [_c_vp, _c_vp, _c_vp]),
     "mm_forward_bf16": (_c_int, [_c_int] * 5 + [_c_vp] * 8 + [ctypes.c_float, _c_int, _c_vp, _c_size, _c_vp]),
@@ -237,6 +238,25 @@ def mm_quantize_mx(src, rows, cols, fmt, dst, dst_sf, stream=None) -> int:
     return lib().mm_quantize_mx(_ptr(src), rows, cols, fmt, _ptr(dst), _ptr(dst_sf), _stream(stream))
 
 
+def mm_prepare_weight_scales(sf, rows, k, out, stream=None) -> int:
+    """UE8M0 scales [rows, k/32] of a weight matrix -> the prepared layout that
+    mm_forward takes for l1_sf / l2_sf (same byte count; see include/megamoe.h)."""
+    return lib().mm_prepare_weight_scales(_ptr(sf), rows, k, _ptr(out), _stream(stream))
+
+
+def prepare_weight_scales(sf, k, stream=None):
+    """Torch convenience: a new tensor holding the prepared scales of `sf`
+    (uint8, rows x k/32 bytes in any shape whose last dimension is k/32)."""
+    import torch
+
+    rows = sf.numel() // (k // 32)
+    out = torch.empty_like(sf, memory_format=torch.contiguous_format)
+    rc = mm_prepare_weight_scales(sf, rows, k, out, stream)
+    if rc != MM_OK:
+        raise MegaMoEError("mm_prepare_weight_scales", rc)
+    return out
+
+
 def mm_forward_noalloc(num_tokens, experts, topk, hidden, inter, x, x_sf, topk_idx, topk_w, l1_w, l1_sf,
                        l2_w, l2_sf, y, clamp, num_sms, stream=None) -> int:
     """mm_forward with the library's fixed 48 MiB device scratch as workspace,
@@ -258,6 +278,8 @@ def mm_noalloc_get_status(stream=None):
 class MegaMoELayer:
     """Resident expert weights plus a caller-owned workspace (torch tensors).
 
+    ``l1_sf`` / ``l2_sf`` are the UE8M0 scales as ``mm_quantize_mx`` writes
+    them; the layer keeps its own prepared copies (mm_prepare_weight_scales).
     ``forward`` enqueues ``mm_forward`` on the current (or given) stream.  All
     arithmetic happens in the library's kernels.
     """
@@ -267,7 +289,9 @@ class MegaMoELayer:
         import torch
 
         self.E, self.k, self.H, self.I = experts, topk, hidden, inter
-        self.l1_w, self.l1_sf, self.l2_w, self.l2_sf = l1_w, l1_sf, l2_w, l2_sf
+        self.l1_w, self.l2_w = l1_w, l2_w
+        self.l1_sf = prepare_weight_scales(l1_sf, hidden)
+        self.l2_sf = prepare_weight_scales(l2_sf, inter)
         self.clamp, self.num_sms = clamp, num_sms
         self.max_tokens = max_tokens
         nbytes = mm_workspace_size(max_tokens, experts, topk, hidden, inter)

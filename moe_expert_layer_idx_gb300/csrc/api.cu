@@ -19,6 +19,8 @@ cudaError_t layer_prepare(int variant, int sms, int* resident);
 cudaError_t layer_launch(int variant, int grid, cudaStream_t stream, const CUtensorMap* maps, const ForwardParams& p);
 cudaError_t launch_quantize(const float* src, long long nblocks, bool e4m3, uint8_t* dst, uint8_t* sf,
                             int grid, cudaStream_t stream);
+cudaError_t launch_prepare_weight_scales(const uint8_t* sf, long long rows, int kb, uint8_t* out, int max_ctas,
+                                         cudaStream_t stream);
 cudaError_t launch_quantize_f8b(const float* src, long long rows, long long cols, int block_rows, uint8_t* dst,
                                 float* sf, int max_ctas, cudaStream_t stream);
 }  // namespace mm
@@ -264,7 +266,8 @@ static int forward_impl(int recipe, int num_tokens, int experts, int topk, int h
     return MM_ERR_INVALID_ARG;
   if ((bf16_layer && !aligned(x, 16)) || (fp8_in && (!aligned(x, 16) || !aligned(x_sf, 4))) ||
       (!bf16_layer && !fp8_in && !aligned(x_bf16, 16)) || !aligned(topk_idx, 4) || !aligned(topk_w, 4) ||
-      !aligned(l1_w, 32) || !aligned(l2_w, 32) || (scales && (!aligned(l1_sf, 4) || !aligned(l2_sf, 4))) ||
+      !aligned(l1_w, 32) || !aligned(l2_w, 32) ||
+      (scales && (!aligned(l1_sf, f8b ? 4 : 16) || !aligned(l2_sf, f8b ? 4 : 16))) ||   // scale atoms: bulk copies
       !aligned(y, 16))
     return MM_ERR_INVALID_ARG;
   if (std::isnan(clamp)) return MM_ERR_INVALID_ARG;
@@ -438,7 +441,8 @@ int mm_workspace_region(int which, int num_tokens, int experts, int topk, int hi
   const size_t C = (size_t)route_ctas((long long)A);
   const size_t exact[15] = {4 * (size_t)kCtrlWords, 4 * (size_t)experts, 4 * (size_t)(experts + 1),
                             4 * (size_t)(experts + 1), 4 * (size_t)experts, 4 * (size_t)experts, 4 * A, 4 * A,
-                            A * hidden, A * (hidden / 32), A * inter, A * (inter / 32), A * hidden * 4,
+                            A * hidden, token_atom_bytes(A, experts, hidden), A * inter,
+                            token_atom_bytes(A, experts, inter), A * hidden * 4,
                             4 * (size_t)experts * C + 4 * C, 16 * A};
   if (offset) *offset = starts[which];
   if (bytes) *bytes = exact[which];
@@ -461,6 +465,20 @@ int mm_quantize_mx(const float* src, long long rows, long long cols, int fmt, vo
   if (blocks > cap) blocks = cap;
   if (launch_quantize(src, nblocks, fmt == MM_FMT_E4M3, static_cast<uint8_t*>(dst), static_cast<uint8_t*>(dst_sf),
                       (int)blocks, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return MM_ERR_CUDA;
+  return MM_OK;
+}
+
+int mm_prepare_weight_scales(const void* sf, long long rows, long long k, void* out, mm_stream_t stream) {
+  if (rows < 0 || k < 0 || rows % 128 != 0 || k % 128 != 0 || k / 32 > (1ll << 30)) return MM_ERR_INVALID_ARG;
+  if (rows * k == 0) return MM_OK;
+  if (!sf || !out || !aligned(sf, 4) || !aligned(out, 16)) return MM_ERR_INVALID_ARG;
+  int dev;
+  DevState* st;
+  int rc = device_state(&dev, &st);
+  if (rc != MM_OK) return rc;
+  if (launch_prepare_weight_scales(static_cast<const uint8_t*>(sf), rows, (int)(k / 32), static_cast<uint8_t*>(out),
+                                   st->sms * 16, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
     return MM_ERR_CUDA;
   return MM_OK;
 }

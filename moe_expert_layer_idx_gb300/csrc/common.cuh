@@ -31,6 +31,25 @@ constexpr int kSFABytes = 512;                      // one 128-row scale atom (t
 constexpr int kSFBBytes = 1024;                     // two 128-row scale atoms (weights)
 constexpr int kBarBytes = 512;                      // mbarriers + small shared state
 
+// ----------------------------------------------------------------- scale atoms
+// The UE8M0 scales of 128 rows for one 128-wide K stage (4 blocks of 32), in
+// the order tcgen05.cp (32x128b, warpx4) copies them into TMEM: 32 lanes of 16
+// bytes, lane l holding the 4 scale bytes of rows l, 32 + l, 64 + l and 96 + l.
+// Byte (row r, block k) of an atom sits at atom_pos(r) + k.  Both operands'
+// scales reach shared memory as whole atoms:
+// * weights: prepared once (mm_prepare_weight_scales) as [row / 128][K / 128]
+//   atoms of a [rows, K/32] scale matrix;
+// * tokens: written by the kernel itself (dispatch, L1 epilogue) as
+//   [token block][128-row half][K / 128] atoms in the workspace.
+constexpr int kAtomBytes = 512;
+__host__ __device__ inline int atom_pos(int r) { return (r & 31) * 16 + (r >> 5) * 4; }
+// Token-scale atoms of a layer with K-dimension K: room for every token block
+// of any layer kernel (at most 2E + A/32 block halves: blocks of >= 32 rows,
+// one half per 128 rows of a block).
+__host__ __device__ inline size_t token_atom_bytes(size_t A, int E, int K) {
+  return (2 * (size_t)E + (A + 31) / 32) * (size_t)(K / 128) * kAtomBytes;
+}
+
 // Tile ring of the dynamic schedule: depth, and the number of roles that read
 // each entry (producer 1, scale loader, MMA issuer, the epilogue warps).
 constexpr int kTileRing = 4;
@@ -90,6 +109,12 @@ struct Variant {
   static constexpr bool kF8B = kF8B_;
   static_assert(!kF8B || (!kBf16 && !kPair && kARows == kTileM && kSub == 1), "the per-128 recipe runs wide tiles");
   static constexpr bool kNoSF = kBf16 || kF8B;         // no block-scale atoms for the MMA
+  // Who moves a stage's scale atoms into shared memory: in the 128-token
+  // tiles (one CTA or a pair) the scale-loader warp, with coalesced loads, so
+  // that the producers issue only the TMA boxes (their issue time per stage is
+  // what limits those tiles; a pair's CTAs also need the weight atoms of both
+  // halves); in the thin tiles the producers, by bulk copies beside the boxes.
+  static constexpr bool kSLWarp = !kNoSF && kSub == 1 && kARows == 128;
   static constexpr int kCtas = kPair ? 2 : 1;          // CTAs that share one MMA tile
   static constexpr int kBlockRows = kARows * kCtas;    // largest token block of a tile
   static constexpr int kKStage = kBf16 ? kBlockK / 2 : kBlockK;     // K elements per stage
@@ -109,7 +134,7 @@ struct Variant {
   static_assert(kARows % 16 == 0 && kARows <= kTileM, "token rows per stage");
   // barriers (2 per stage, 3 accumulator/drain, 2 per tile-ring slot, 4 partial-accumulator),
   // misc words, votes, tile ring
-  static_assert((2 * kStages + 3 + 2 * kTileRing + 4) * 8 + 8 * 4 + 2 * kEpiWarps * 4 + kTileRing * 9 * 4 <= kBarBytes,
+  static_assert((2 * kStages + 3 + 2 * kTileRing + 4) * 8 + 8 * 4 + 2 * kEpiWarps * 4 + kTileRing * 10 * 4 <= kBarBytes,
                 "barrier region");
   static_assert(kSFCol0 + kStages * kSub * kSFSetCols <= kTmemCols, "scale-factor sets fit TMEM");
   // the MMA's 128-row A window of the last sub-stage stays inside the allocation
@@ -176,9 +201,10 @@ __host__ __device__ inline Layout make_layout(long long T, int E, int k, int H, 
   L.perm = o;     o = align256(o + 4 * A);
   L.inv = o;      o = align256(o + 4 * A);
   L.xs = o;       o = align256(o + A * (size_t)H * esz);
-  L.xs_sf = o;    o = align256(o + A * (size_t)(H / 32));
+  // (E4M3 x E2M1: scale atoms; the (1, 128, 128) recipe: fp32 scales per slot row, which fit too)
+  L.xs_sf = o;    o = align256(o + token_atom_bytes(A, E, H));
   L.l1a = o;      o = align256(o + A * (size_t)I * esz);
-  L.l1a_sf = o;   o = align256(o + A * (size_t)(I / 32));
+  L.l1a_sf = o;   o = align256(o + token_atom_bytes(A, E, I));
   L.stage = o;    o = align256(o + A * (size_t)H * 4);
   // per-chunk expert counts, then base slots, [E][C] int32, and one bad-index word per chunk
   const size_t C = (size_t)route_ctas((long long)A);
@@ -409,6 +435,15 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3}], [%4];"
       :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+// Contiguous bytes global -> this CTA's shared memory (bulk copy, async proxy),
+// completing on one of this CTA's barriers; addresses 16-byte aligned, bytes a
+// multiple of 16.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      :: "r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
       : "memory");
 }
 // TMA into this CTA's shared memory, completing on a barrier of either CTA of

@@ -66,6 +66,7 @@ struct Tile {
   int n;       // MMA N: 256, or 128 for a hidden tail
   int ks;      // K stages
   int tag;     // tile index (reported with a wait that gives up)
+  int blk;     // global index of the token block (its scale atoms)
 };
 
 // Tiles are numbered L1 first, then L2; within a layer expert-major, then the
@@ -94,6 +95,27 @@ __device__ __forceinline__ void decode_tile(int t, int nL1, const ForwardParams&
   ti.n = l1 ? kTileN : min(kTileN, p.H - nb * kTileN);
   ti.ks = l1 ? p.ks1 : p.ks2;
   ti.tag = t & 0xFFFFFF;
+  ti.blk = i0 + mb;
+}
+
+// Where slot s's row sits among a layer's token-scale atoms (slot s belongs to
+// expert e; token blocks as the routing kernels made them: n_blocks(count,
+// max_rows) balanced blocks per expert, `halves` 128-row halves each), packed
+// as (block half << 9) | byte position within the atom; the byte offset of
+// stage j is then atom_offset(packed, S) + j * kAtomBytes (S stages per row).
+__device__ __forceinline__ uint32_t token_atom_slot(const ForwardParams& p, const int32_t* items,
+                                                    const int32_t* counts, const int32_t* offsets, int e, int s,
+                                                    int halves) {
+  const int cnt = __ldg(counts + e);
+  const int mbk = n_blocks(cnt, p.max_rows);
+  const int rpb = (cnt + mbk - 1) / mbk;
+  const int i = s - __ldg(offsets + e);
+  const int mb = i / rpb, row = i - mb * rpb;
+  const int b = __ldg(items + e) + mb;
+  return ((uint32_t)(b * halves + (row >> 7)) << 9) | (uint32_t)atom_pos(row & 127);
+}
+__device__ __forceinline__ size_t atom_offset(uint32_t packed, int S) {
+  return (size_t)(packed >> 9) * S * kAtomBytes + (packed & 511u);
 }
 
 // Dynamic tile schedule.  Producer 0 claims the next tile index from a global
@@ -262,7 +284,7 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       // producers (+ the scale loader), of both CTAs of a pair
-      mbar_init(&full[s], (V::kNoSF ? 2 : 2 + 1) * G);
+      mbar_init(&full[s], (V::kSLWarp ? 2 + 1 : 2) * G);
       mbar_init(&empty[s], 1);
     }
     mbar_init(tfull, 1);
@@ -309,43 +331,52 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
     const int H = p.H, k = p.k, nblk = H / 32;
     for (int t = blockIdx.x * (kThreads / 32) + warp; t < p.T; t += gridDim.x * (kThreads / 32)) {
       int my_e = -1, my_slot = -1;                   // lane j < k: slot j of the token
+      uint32_t my_atom = 0;                          // and its row's place among the scale atoms
       if (lane < k) {
         my_e = __ldg(p.topk_idx + (size_t)t * k + lane);
-        if (my_e >= 0) my_slot = __ldg(inv + (size_t)t * k + lane);
-      }
-      int slots[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j) slots[j] = __shfl_sync(0xffffffffu, my_slot, j);
-      const uint4* src = reinterpret_cast<const uint4*>(p.x_bf16 + (size_t)t * H);
-      for (int b = lane; b < nblk; b += 32) {
-        float v[32];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint4 q = __ldg(src + 4 * b + c);
-          const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            v[8 * c + 2 * i] = __uint_as_float(w[i] << 16);             // bf16 -> fp32 is exact
-            v[8 * c + 2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-          }
+        if (my_e >= 0) {
+          my_slot = __ldg(inv + (size_t)t * k + lane);
+          my_atom = token_atom_slot(p, items, counts, offsets, my_e, my_slot, V::kCtas);
         }
-        float a = 0.f;
+      }
+      const uint4* src = reinterpret_cast<const uint4*>(p.x_bf16 + (size_t)t * H);
+      // every lane runs the same iterations, so slot j's row and atom place can be
+      // fetched from lane j by a shuffle at the point of use
+      for (int b0 = 0; b0 < nblk; b0 += 32) {
+        const int b = b0 + lane;
+        const bool act = b < nblk;
+        uint32_t w[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+        int sc = 0;
+        if (act) {
+          float v[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) a = fmaxf(a, fabsf(v[i]));
-        const int sc = block_scale_exp<true>(a);
-        const float inv_s = exp2_neg(sc);
-        uint32_t w[8];
+          for (int c = 0; c < 4; ++c) {
+            const uint4 q = __ldg(src + 4 * b + c);
+            const uint32_t u4[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-          w[i] = e4m3_code(v[4 * i] * inv_s) | (e4m3_code(v[4 * i + 1] * inv_s) << 8) |
-                 (e4m3_code(v[4 * i + 2] * inv_s) << 16) | (e4m3_code(v[4 * i + 3] * inv_s) << 24);
+            for (int i = 0; i < 4; ++i) {
+              v[8 * c + 2 * i] = __uint_as_float(u4[i] << 16);             // bf16 -> fp32 is exact
+              v[8 * c + 2 * i + 1] = __uint_as_float(u4[i] & 0xFFFF0000u);
+            }
+          }
+          float a = 0.f;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          if (j < k && slots[j] >= 0) {
-            uint4* d4 = reinterpret_cast<uint4*>(xs + (size_t)slots[j] * H + 32 * b);
+          for (int i = 0; i < 32; ++i) a = fmaxf(a, fabsf(v[i]));
+          sc = block_scale_exp<true>(a);
+          const float inv_s = exp2_neg(sc);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            w[i] = e4m3_code(v[4 * i] * inv_s) | (e4m3_code(v[4 * i + 1] * inv_s) << 8) |
+                   (e4m3_code(v[4 * i + 2] * inv_s) << 16) | (e4m3_code(v[4 * i + 3] * inv_s) << 24);
+        }
+        for (int j = 0; j < k; ++j) {
+          const int slot = __shfl_sync(0xffffffffu, my_slot, j);
+          const uint32_t at = __shfl_sync(0xffffffffu, my_atom, j);
+          if (act && slot >= 0) {
+            uint4* d4 = reinterpret_cast<uint4*>(xs + (size_t)slot * H + 32 * b);
             d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
             d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
-            xs_sf[(size_t)slots[j] * nblk + b] = (uint8_t)(sc + 127);
+            xs_sf[atom_offset(at, H / 128) + (size_t)(b >> 2) * kAtomBytes + (b & 3)] = (uint8_t)(sc + 127);
           }
         }
       }
@@ -387,10 +418,16 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
           for (int i = 0; i < 16; ++i)
             if (c0 + 32 * i < nvec) dst[c0 + 32 * i] = v[i];
         }
-        if (!V::kBf16) {
+        if constexpr (V::kF8B) {
+          // fp32 scale per 128 elements: rows of H / 32 bytes, in slot order
           const uint32_t* ssf = reinterpret_cast<const uint32_t*>(p.x_sf + (size_t)t * (H / 32));
           uint32_t* dsf = reinterpret_cast<uint32_t*>(xs_sf + (size_t)s * (H / 32));
           for (int c = lane; c < nsf; c += 32) dsf[c] = __ldg(ssf + c);
+        } else if constexpr (!V::kBf16) {
+          // the 4 UE8M0 bytes of stage c go to the row's place in the block's stage-c atom
+          const uint32_t* ssf = reinterpret_cast<const uint32_t*>(p.x_sf + (size_t)t * (H / 32));
+          uint8_t* da = xs_sf + atom_offset(token_atom_slot(p, items, counts, offsets, es[u], s, V::kCtas), nsf);
+          for (int c = lane; c < nsf; c += 32) *reinterpret_cast<uint32_t*>(da + (size_t)c * kAtomBytes) = __ldg(ssf + c);
         }
       }
       fence_proxy_async_global();
@@ -454,13 +491,20 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
         const int nbox = m16 / 16;
         const int my_a_bytes = full_box ? (pid == box_pid ? kABytes : 0) : ((nbox + 1 - pid) / 2) * 16 * kBlockK;
         const bool my_b = V::kPair ? pid == 0 : (pid == 0 || ti.n > 128);
-        const uint32_t bytes = (uint32_t)((my_b ? V::kWeightBoxTx : 0) + my_a_bytes);
+        // scale atoms by bulk copy: each producer its weight half's atoms, producer 1 the token atoms
+        // (producer 0 issues the single 128-row token box)
+        constexpr bool kAtoms = !V::kNoSF && !V::kSLWarp;
+        const int sf_bytes = kAtoms ? (my_b ? kAtomBytes : 0) + (pid == 1 ? kAtomBytes : 0) : 0;
+        const uint32_t bytes = (uint32_t)((my_b ? V::kWeightBoxTx : 0) + my_a_bytes + sf_bytes);   // per K stage
         const CUtensorMap* tm_b = ti.layer == 1 ? &tm_w1 : &tm_w2;
         const CUtensorMap* tm_a = ti.layer == 1 ? (full_box ? &tm_xs128 : &tm_xs16)
                                                 : (full_box ? &tm_l1a128 : &tm_l1a16);
         const int bsel = V::kPair ? (int)crank : pid;             // which 128-row half of the weight tile
         const int b_row = ti.layer == 1 ? ti.e * 2 * p.I + ti.nb * kL1Feat + bsel * p.I
                                         : ti.e * p.H + ti.nb * kTileN + bsel * 128;
+        // stage 0 of this tile's weight-half atoms ([row / 128][K / 128]) and token atoms ([block][K / 128])
+        const uint8_t* w_atoms = (ti.layer == 1 ? p.w1_sf : p.w2_sf) + (size_t)(b_row / 128) * ti.ks * kAtomBytes;
+        const uint8_t* t_atoms = (ti.layer == 1 ? xs_sf : l1a_sf) + (size_t)ti.blk * ti.ks * kAtomBytes;
         for (int kk0 = 0; kk0 < ti.ks; kk0 += kSub) {
           const int nsub = min(kSub, ti.ks - kk0);
           if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, ctrl, to, (kSiteEmpty << 24) | tag)) { ok = false; break; }
@@ -468,6 +512,15 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
           const uint32_t fbar = V::kPair ? cluster_addr(fb, 0) : fb;
           if constexpr (V::kPair) mbar_arrive_expect_tx_cluster(fbar, bytes * (uint32_t)nsub);
           else mbar_arrive_expect_tx(fbar, bytes * (uint32_t)nsub);
+          if constexpr (kAtoms) {
+            // the slot's nsub stages of an atom sequence are contiguous on both sides
+            const uint32_t nb_sf = (uint32_t)(nsub * kAtomBytes);
+            if (my_b)
+              bulk_load(smem_u32(sSFB + stage * kSub * kSFBBytes + bsel * kSub * kAtomBytes),
+                        w_atoms + (size_t)kk0 * kAtomBytes, nb_sf, fbar);
+            if (pid == 1)
+              bulk_load(smem_u32(sSFA + stage * kSub * kSFABytes), t_atoms + (size_t)kk0 * kAtomBytes, nb_sf, fbar);
+          }
           for (int u = 0; u < nsub; ++u) {
             const int gs = stage * kSub + u;
             const uint32_t a_dst = smem_u32(sA + gs * kABytes);
@@ -549,11 +602,12 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
               tc_mma_f16(tmem, ad + 4, bd + 4, idb, 1u);
               tc_mma_f16(tmem, ad + 6, bd + 6, idb, 1u);
             } else {
-              const uint64_t sfb_d = sfb_desc0 + (uint64_t)(so * (uint32_t)(kSFBBytes >> 4));
+              // a slot's weight atoms: [128-row half][sub-stage]
+              const uint64_t sfb_d = sfb_desc0 + (uint64_t)((stage * kSub * kSFBBytes + u * kAtomBytes) >> 4);
               const uint32_t sfa_t = tmem + kSFCol0 + so * kSFSetCols, sfb_t = sfa_t + 4;
               tc_cp_sf<G>(sfa_t, sfa_desc0 + (uint64_t)(so * (uint32_t)(kSFABytes >> 4)));
               tc_cp_sf<G>(sfb_t, sfb_d);
-              if (two_sfb) tc_cp_sf<G>(sfb_t + 4, sfb_d + (512 >> 4));
+              if (two_sfb) tc_cp_sf<G>(sfb_t + 4, sfb_d + (uint64_t)((kSub * kAtomBytes) >> 4));
               tc_mma_mx<G>(tmem, ad, bd, id0, sfa_t, sfb_t, acc0);
               tc_mma_mx_acc<G>(tmem, ad + 2, bd + 2, id1, sfa_t, sfb_t);   // K = 32 each: +32 bytes
               tc_mma_mx_acc<G>(tmem, ad + 4, bd + 4, id2, sfa_t, sfb_t);
@@ -576,30 +630,27 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
       tc_commit<G>(smem_u32(drain));
       if (!mbar_wait_drain(smem_u32(drain), 0, to)) set_error(ctrl, MM_ERR_TIMEOUT, kSiteDrain << 24);
     }
-  } else if (warp == 2 && V::kNoSF) {
-    // ---------------- no scale factors in the bf16 layer: only follow the tile feed
+  } else if (warp == 2 && !V::kSLWarp) {
+    // ---------------- scale atoms come with the TMA loads (or there are none): only follow the tile feed
     TileFeed feed(s_tiles, tile_full, tile_empty);
     bool fed = true;
     Tile ti;
     while (feed.take_warp(lane, ctrl, to, fed, ti)) {}
   } else if (warp == 2) {
+   if constexpr (V::kSLWarp) {
     // ---------------- scale loader (32 lanes)
-    // Lane l owns rows l + 32j of the tile's token block (j < 4) and of its
-    // weight rows (two 128-row atoms).  For every group of 4 K stages it loads
-    // each owned row's 4 x 4 scale bytes (16 contiguous bytes: one vector load
-    // where rows are 16-byte aligned) into registers, ahead of the stages.
-    // Then, stage by stage, it writes the stage's bytes into the 32x4x4 atom
-    // layout (one 16-byte shared store per atom and lane), every lane fences
-    // them (the tensor core reads through the async proxy) and lane 0 arrives
-    // on the stage's full barrier.  In a pair each CTA writes the atoms of its
-    // own token rows and both weight atoms (the MMA reads the weight scales of
-    // all 256 rows from each CTA's TMEM), and arrives on the even CTA's barrier.
+    // Copies, stage by stage, the token atom of this CTA's 128 rows of the
+    // block and the weight atoms of both 128-row halves of the tile into
+    // shared memory (in a pair each CTA holds all 256 rows' weight scales: the
+    // MMA reads them from each CTA's TMEM); lane l moves bytes [16l, 16l + 16)
+    // of each atom, the loads of 4 stages in flight at a time.  Every lane
+    // fences its stores (the tensor core reads through the async proxy) and
+    // lane 0 arrives on the full barrier (in a pair, the even CTA's).
     uint32_t stage = 0, phase = 0, armed = 0;
     int ready_key = -1;
-    const int H32 = p.H / 32, I32 = p.I / 32;
     TileFeed feed(s_tiles, tile_full, tile_empty);
     if constexpr (V::kPair) feed.pair(crank);
-    const uint32_t full0_cl = V::kPair ? cluster_addr(smem_u32(&full[0]), 0) : 0u;
+    const uint32_t full0 = V::kPair ? cluster_addr(smem_u32(&full[0]), 0) : smem_u32(&full[0]);
     for (;;) {
       bool fed = true;
       Tile ti;
@@ -617,83 +668,45 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         __syncwarp();
-        // every lane acquires the producers' writes before reading them
+        // every lane acquires the writers' atoms before reading them
         if (ti.layer == 1) (void)ld_acquire(&arrival[ti.e]); else (void)ld_acquire(&l1_done[ti.e]);
         ready_key = key;
       }
-      const uint8_t* a_sf_base = ti.layer == 1 ? xs_sf : l1a_sf;
-      const uint8_t* b_sf_base = ti.layer == 1 ? p.w1_sf : p.w2_sf;
-      const int kstride = ti.layer == 1 ? H32 : I32;
+      const int S = ti.ks;
       const int b_row0 = ti.layer == 1 ? ti.e * 2 * p.I + ti.nb * kL1Feat : ti.e * p.H + ti.nb * kTileN;
       const int b_row1 = ti.layer == 1 ? b_row0 + p.I : b_row0 + 128;
-      const bool two_sfb = ti.n > 128;
-      const bool a_vec = (kstride & 15) == 0;                                    // workspace rows
-      const bool b_vec = a_vec && (reinterpret_cast<uintptr_t>(b_sf_base) & 15) == 0;
-      const int tr = (int)crank * kTileM;                        // this CTA's first row of the block
-      const int m16 = (max(0, min(ti.rows - tr, kTileM)) + 15) & ~15;
-      const int r0 = ti.r0 + tr;
-      const uint8_t* a_row[4];
-      const uint8_t* b_row[8];
+      const uint8_t* wsf = ti.layer == 1 ? p.w1_sf : p.w2_sf;
+      const uint8_t* ta = (ti.layer == 1 ? xs_sf : l1a_sf) + ((size_t)(ti.blk * V::kCtas + (int)crank) * S) * kAtomBytes +
+                          lane * 16;
+      const uint8_t* tb0 = wsf + (size_t)(b_row0 / 128) * S * kAtomBytes + lane * 16;
+      const uint8_t* tb1 = wsf + (size_t)((ti.n > 128 ? b_row1 : b_row0) / 128) * S * kAtomBytes + lane * 16;
+      for (int g0 = 0; g0 < S && ok; g0 += 4) {
+        const int ng = min(4, S - g0);
+        uint4 a[4], b0[4], b1[4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int slot = min(r0 + lane + 32 * j, p.A - 1);
-        a_row[j] = a_sf_base + (size_t)slot * kstride;
-        b_row[j] = b_sf_base + (size_t)(b_row0 + lane + 32 * j) * kstride;
-        b_row[4 + j] = b_sf_base + (size_t)((two_sfb ? b_row1 : b_row0) + lane + 32 * j) * kstride;
-      }
-      for (int g0 = 0; g0 < ti.ks && ok; g0 += 4) {
-        const int ng = min(4, ti.ks - g0);
-        uint32_t a[4][4], b[8][4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          if (lane + 32 * j < m16) {
-            if (a_vec && ng == 4) {
-              const uint4 v = __ldcg(reinterpret_cast<const uint4*>(a_row[j] + g0 * 4));
-              a[j][0] = v.x; a[j][1] = v.y; a[j][2] = v.z; a[j][3] = v.w;
-            } else {
-#pragma unroll
-              for (int q = 0; q < 4; ++q)
-                a[j][q] = q < ng ? __ldcg(reinterpret_cast<const uint32_t*>(a_row[j] + (g0 + q) * 4)) : 0u;
-            }
-          } else {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) a[j][q] = 0u;       // rows past the block: unused accumulator lanes
+        for (int q = 0; q < 4; ++q) {
+          if (q < ng) {
+            const size_t o = (size_t)(g0 + q) * kAtomBytes;
+            a[q] = __ldcg(reinterpret_cast<const uint4*>(ta + o));
+            b0[q] = __ldg(reinterpret_cast<const uint4*>(tb0 + o));
+            b1[q] = __ldg(reinterpret_cast<const uint4*>(tb1 + o));
           }
         }
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          if (b_vec && ng == 4) {
-            const uint4 v = __ldg(reinterpret_cast<const uint4*>(b_row[j] + g0 * 4));
-            b[j][0] = v.x; b[j][1] = v.y; b[j][2] = v.z; b[j][3] = v.w;
-          } else {
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-              b[j][q] = q < ng ? __ldg(reinterpret_cast<const uint32_t*>(b_row[j] + (g0 + q) * 4)) : 0u;
-          }
-        }
-#pragma unroll
-        for (int q = 0; q < 4; q += kSub) {                  // one ring slot: K stages g0 + q .. + kSub - 1
+        for (int q = 0; q < 4; ++q) {
           if (q >= ng) break;
           bool w = true;
           if (lane == 0) w = mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, ctrl, to, (kSiteEmpty << 24) | tag);
           w = __shfl_sync(0xffffffffu, w, 0);
           if (!w) { ok = false; break; }
-#pragma unroll
-          for (int u = 0; u < kSub; ++u) {
-            if (q + u < ng) {
-              const int gs = stage * kSub + u;
-              uint4* dA = reinterpret_cast<uint4*>(sSFA + gs * kSFABytes) + lane;
-              uint4* dB = reinterpret_cast<uint4*>(sSFB + gs * kSFBBytes) + lane;
-              *dA = make_uint4(a[0][q + u], a[1][q + u], a[2][q + u], a[3][q + u]);
-              dB[0] = make_uint4(b[0][q + u], b[1][q + u], b[2][q + u], b[3][q + u]);
-              dB[32] = make_uint4(b[4][q + u], b[5][q + u], b[6][q + u], b[7][q + u]);
-            }
-          }
+          reinterpret_cast<uint4*>(sSFA + stage * kSFABytes)[lane] = a[q];
+          reinterpret_cast<uint4*>(sSFB + stage * kSFBBytes)[lane] = b0[q];
+          reinterpret_cast<uint4*>(sSFB + stage * kSFBBytes + kAtomBytes)[lane] = b1[q];
           fence_proxy_async_shared();
           __syncwarp();
           if (lane == 0) {
-            if constexpr (V::kPair) mbar_arrive_cluster(full0_cl + stage * 8u);
-            else mbar_arrive(smem_u32(&full[stage]));
+            if constexpr (V::kPair) mbar_arrive_cluster(full0 + stage * 8u);
+            else mbar_arrive(full0 + stage * 8u);
           }
           ++armed;
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
@@ -702,6 +715,7 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
       if (!ok) break;
     }
     if (lane == 0) s_misc[4] = armed;
+   }
   } else {
     // ---------------- epilogue: warp w reads TMEM lanes 32q..32q+31 (token rows), q = w % 4;
     // the warps w < 8 and w >= 8 of a quarter take the first and second half of the columns
@@ -917,9 +931,9 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
             }
             sfw |= (uint32_t)(s + 127) << (8 * bi);
           }
-          if (valid)
-            *reinterpret_cast<uint16_t*>(l1a_sf + slot * (p.I / 32) + ti.nb * (kL1Feat / 32) + 2 * hh) =
-                (uint16_t)sfw;
+          if (valid)   // bytes 2hh, 2hh + 1 of the row in the block's atom of L2 stage nb
+            *reinterpret_cast<uint16_t*>(l1a_sf + ((size_t)(ti.blk * V::kCtas + (int)crank) * (p.I / 128) + ti.nb) * kAtomBytes +
+                                         atom_pos(row) + 2 * hh) = (uint16_t)sfw;
         } else {
           // ---- L2: this warp's nh output columns x top-k weight -> fp32 row of the flat assignment
           int f = 0;
@@ -1003,7 +1017,7 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
     uint32_t cnt[3 * G];
     cnt[0] = s_misc[2];
     cnt[1] = s_misc[5];
-    cnt[2] = V::kNoSF ? 0xFFFFFFFFu : s_misc[4];
+    cnt[2] = V::kSLWarp ? s_misc[4] : 0xFFFFFFFFu;
     if constexpr (V::kPair) {
       const uint32_t misc_peer = cluster_addr(smem_u32(s_misc), 1);
       cnt[3] = ld_cluster_u32(misc_peer + 4 * 2);

@@ -132,6 +132,36 @@ cudaError_t launch_quantize_f8b(const float* src, long long rows, long long cols
   return cudaGetLastError();
 }
 
+// Weight scales -> scale atoms: a UE8M0 matrix [rows, kb] (kb = K / 32 blocks
+// per row) becomes [rows / 128][kb / 4] atoms of 512 bytes, atom (rb, s) lane
+// l holding the 4 bytes of stage s (blocks 4s .. 4s + 3) of rows 128 rb + l,
+// + 32 + l, + 64 + l and + 96 + l.  One thread per 16-byte lane of an atom.
+__global__ void __launch_bounds__(256) prepare_weight_scales_kernel(const uint8_t* __restrict__ sf, long long rows,
+                                                                    int kb, uint8_t* __restrict__ out) {
+  const int stages = kb / 4;
+  const long long nlanes = rows / 128 * stages * 32;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < nlanes; i += stride) {
+    const int l = (int)(i & 31);
+    const long long atom = i >> 5;                     // rb * stages + s
+    const long long rb = atom / stages;
+    const int s = (int)(atom - rb * stages);
+    const uint8_t* src = sf + (size_t)(rb * 128 + l) * kb + 4 * s;
+    uint32_t w[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) w[c] = __ldg(reinterpret_cast<const uint32_t*>(src + (size_t)c * 32 * kb));
+    reinterpret_cast<uint4*>(out)[i] = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+cudaError_t launch_prepare_weight_scales(const uint8_t* sf, long long rows, int kb, uint8_t* out, int max_ctas,
+                                         cudaStream_t stream) {
+  const long long nlanes = rows / 128 * (kb / 4) * 32;
+  const long long ctas = std::min<long long>((nlanes + 255) / 256, max_ctas);
+  prepare_weight_scales_kernel<<<(int)std::max(1ll, ctas), 256, 0, stream>>>(sf, rows, kb, out);
+  return cudaGetLastError();
+}
+
 // Host launcher (kept in this translation unit: template kernels are launched
 // where they are defined).
 cudaError_t launch_quantize(const float* src, long long nblocks, bool e4m3, uint8_t* dst, uint8_t* sf,

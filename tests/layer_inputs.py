@@ -33,23 +33,28 @@ def gpu_quantize(src: torch.Tensor, rows: int, cols: int, fmt: int, out=None, ou
 
 
 class GpuWeights:
+    """Quantised expert weights; l1_sf / l2_sf hold the prepared scales that
+    mm_forward takes, l1_sf_rows / l2_sf_rows the quantiser's row layout."""
+
     def __init__(self, cfg, device="cuda", chunk=8):
         E, H, I = cfg.E, cfg.H, cfg.I
         self.l1_w = torch.empty(E, 2 * I, H // 2, dtype=torch.uint8, device=device)
-        self.l1_sf = torch.empty(E, 2 * I, H // 32, dtype=torch.uint8, device=device)
+        self.l1_sf_rows = torch.empty(E, 2 * I, H // 32, dtype=torch.uint8, device=device)
         self.l2_w = torch.empty(E, H, I // 2, dtype=torch.uint8, device=device)
-        self.l2_sf = torch.empty(E, H, I // 32, dtype=torch.uint8, device=device)
+        self.l2_sf_rows = torch.empty(E, H, I // 32, dtype=torch.uint8, device=device)
         n1, n2 = 2 * I * H, H * I
         buf = torch.empty(min(chunk, E) * n1, dtype=torch.float32, device=device)
         for e0 in range(0, E, chunk):
             e1 = min(E, e0 + chunk)
             b = buf[: (e1 - e0) * n1]
             synth.normal_f32_cuda(cfg.seed, synth.TENSOR_W1, e0 * n1, b, synth.weight_scale(H))
-            gpu_quantize(b, (e1 - e0) * 2 * I, H, mm.MM_FMT_E2M1, self.l1_w[e0:e1], self.l1_sf[e0:e1])
+            gpu_quantize(b, (e1 - e0) * 2 * I, H, mm.MM_FMT_E2M1, self.l1_w[e0:e1], self.l1_sf_rows[e0:e1])
             b = buf[: (e1 - e0) * n2]
             synth.normal_f32_cuda(cfg.seed, synth.TENSOR_W2, e0 * n2, b, synth.weight_scale(I))
-            gpu_quantize(b, (e1 - e0) * H, I, mm.MM_FMT_E2M1, self.l2_w[e0:e1], self.l2_sf[e0:e1])
+            gpu_quantize(b, (e1 - e0) * H, I, mm.MM_FMT_E2M1, self.l2_w[e0:e1], self.l2_sf_rows[e0:e1])
         del buf
+        self.l1_sf = mm.prepare_weight_scales(self.l1_sf_rows, H)
+        self.l2_sf = mm.prepare_weight_scales(self.l2_sf_rows, I)
         torch.cuda.synchronize(device)
 
 
@@ -101,6 +106,56 @@ def run_layer(cfg, w: GpuWeights, tok: GpuTokens, num_sms=0, clamp=None, workspa
     st, sm, info = mm.mm_get_status(workspace, stream)
     assert st == mm.MM_OK, (mm.STATUS_NAMES.get(st, st), sm, hex(info))
     return y, workspace
+
+
+# token rows per block of each layer variant (mm_layer_variant's numbering)
+BLOCK_ROWS = {0: 128, 1: 32, 2: 128, 3: 32, 4: 256}
+
+
+def atom_pos(r):
+    """Byte of row r (< 128) within a 512-byte scale atom (lane r % 32, word r / 32)."""
+    r = np.asarray(r)
+    return (r % 32) * 16 + (r // 32) * 4
+
+
+def token_scale_rows(ws: torch.Tensor, cfg, which: str, variant: int, idx=None) -> np.ndarray:
+    """The UE8M0 token scales a forward left in the workspace ("xs_sf": the
+    dispatched x scales, K = H; "l1_acts_sf": the L1 activation scales, K = I),
+    read back from their atoms into rows [n_valid, K/32] in slot order."""
+    from oracle.routing import route
+
+    T, E, k, H, I = cfg.T, cfg.E, cfg.k, cfg.H, cfg.I
+    K = H if which == "xs_sf" else I
+    S = K // 128
+    idx = np.asarray(cfg_routing_idx(cfg) if idx is None else idx)
+    counts, offsets, _, _ = route(idx, E)
+    rows_max = BLOCK_ROWS[variant]
+    halves = 2 if variant == 4 else 1
+    nb = -(-counts // rows_max)
+    first = np.concatenate([[0], np.cumsum(nb)])
+    n = int(offsets[-1])
+    off, nbytes = mm.mm_workspace_region(which, max(T, 1), E, k, H, I)
+    raw = ws[off:off + nbytes].cpu().numpy()
+    out = np.zeros((n, K // 32), np.uint8)
+    for e in range(E):
+        c = int(counts[e])
+        if c == 0:
+            continue
+        mbk = int(nb[e])
+        rpb = -(-c // mbk)
+        i = np.arange(c)
+        mb, row = i // rpb, i % rpb
+        b = first[e] + mb
+        base = ((b * halves + row // 128) * S) * 512 + atom_pos(row % 128)
+        for s in range(S):
+            for j in range(4):
+                out[offsets[e] + i, 4 * s + j] = raw[base + s * 512 + j]
+    return out
+
+
+def cfg_routing_idx(cfg):
+    idx, _, _ = synth.routing(cfg)
+    return idx
 
 
 def bf16_to_np(y: torch.Tensor) -> np.ndarray:

@@ -102,10 +102,11 @@ def test_workspace_size_depends_on_shape_only(lib):
     a = mm.mm_workspace_size(128, 256, 8, 7168, 2048)
     assert a > 0
     assert mm.mm_workspace_size(129, 256, 8, 7168, 2048) > a
-    # the dispatched tokens, L1 activations and weighted L2 rows dominate
-    A = 128 * 8
-    assert a >= A * (7168 + 7168 // 32 + 2048 + 2048 // 32 + 4 * 7168)
-    assert a < A * (7168 + 7168 // 32 + 2048 + 2048 // 32 + 4 * 7168) + 64 * 1024
+    # the dispatched tokens, L1 activations, weighted L2 rows and the token-scale
+    # atoms (room for 2E + A/32 block halves per 128-wide K stage) dominate
+    A, E = 128 * 8, 256
+    big = A * (7168 + 2048 + 4 * 7168) + (2 * E + A // 32) * (7168 // 128 + 2048 // 128) * 512
+    assert big <= a < big + 64 * 1024
 
 
 @pytest.mark.parametrize("args", [(16, 8, 2, 100, 128), (16, 8, 2, 256, 64), (16, 0, 2, 256, 128),
@@ -159,6 +160,7 @@ def test_forward_argument_errors(lib):
     assert _fwd(y=0) == mm.MM_ERR_INVALID_ARG
     assert _fwd(x=FAKE + 8) == mm.MM_ERR_INVALID_ARG            # x needs 16-byte alignment
     assert _fwd(l1_w=FAKE + 16) == mm.MM_ERR_INVALID_ARG        # packed FP4 weights need 32
+    assert _fwd(l2_sf=FAKE + 4) == mm.MM_ERR_INVALID_ARG        # prepared scales need 16 (bulk copies)
     assert _fwd(workspace=FAKE + 128) == mm.MM_ERR_INVALID_ARG  # workspace needs 256
     assert _fwd(clamp=math.nan) == mm.MM_ERR_INVALID_ARG
     need = mm.mm_workspace_size(64, 8, 2, 256, 128)
@@ -242,3 +244,14 @@ def test_layer_variant_choice(lib):
         assert mm.mm_layer_variant(-1, 8, 2, 256) == mm.MM_ERR_INVALID_ARG
     finally:
         mm.mm_set_pair_mma(prev)
+
+
+def test_prepare_weight_scales_argument_errors(lib):
+    """Rows and K must be multiples of 128 and the buffers aligned; checked
+    before any device work (nothing is dereferenced here)."""
+    assert mm.mm_prepare_weight_scales(FAKE, 0, 256, FAKE, stream=0) == mm.MM_OK       # nothing to do
+    assert mm.mm_prepare_weight_scales(FAKE, 100, 256, FAKE, stream=0) == mm.MM_ERR_INVALID_ARG
+    assert mm.mm_prepare_weight_scales(FAKE, 128, 192, FAKE, stream=0) == mm.MM_ERR_INVALID_ARG
+    assert mm.mm_prepare_weight_scales(FAKE + 2, 128, 256, FAKE, stream=0) == mm.MM_ERR_INVALID_ARG
+    assert mm.mm_prepare_weight_scales(FAKE, 128, 256, FAKE + 8, stream=0) == mm.MM_ERR_INVALID_ARG
+    assert mm.mm_prepare_weight_scales(0, 128, 256, FAKE, stream=0) == mm.MM_ERR_INVALID_ARG

@@ -9,7 +9,7 @@ import moe_expert_layer_idx_gb300 as mm
 import synth
 from oracle import formats as OF
 from oracle import moe as OM
-from layer_inputs import (ExpertCache, GpuTokens, GpuWeights, bf16_to_np, close_enough, oracle_tokens,
+from layer_inputs import (ExpertCache, GpuTokens, GpuWeights, bf16_to_np, close_enough, oracle_tokens, token_scale_rows,
                           run_layer)
 
 pytestmark = pytest.mark.gpu
@@ -89,9 +89,9 @@ def test_l1_activations_close_to_oracle(case):
     rounding tie (or a block scale near a power of two); nothing more."""
     cfg, w, tok, y, ws, ref, inter = case
     off, nb = mm.mm_workspace_region("l1_acts", cfg.T, cfg.E, cfg.k, cfg.H, cfg.I)
-    soff, snb = mm.mm_workspace_region("l1_acts_sf", cfg.T, cfg.E, cfg.k, cfg.H, cfg.I)
     codes = ws[off:off + nb].view(cfg.T * cfg.k, cfg.I).cpu().numpy()
-    sfs = ws[soff:soff + snb].view(cfg.T * cfg.k, cfg.I // 32).cpu().numpy()
+    variant = mm.mm_layer_variant(cfg.T, cfg.E, cfg.k, cfg.H)
+    sfs = token_scale_rows(ws, cfg, "l1_acts_sf", variant, idx=tok.idx_np)
     inv = inter["inv"]
     same = total = 0
     for f, (oc, osf) in inter["l1"].items():

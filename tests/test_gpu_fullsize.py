@@ -29,7 +29,7 @@ from oracle import moe as OM
 from oracle.routing import route
 from helpers import blocker
 from layer_inputs import (TOL_NL2, ExpertCache, GpuTokens, GpuWeights, bf16_to_np, close_enough, oracle_tokens,
-                          run_layer)
+                          run_layer, token_scale_rows)
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -109,10 +109,9 @@ def _dense_expert_parity(cfg, ws, tok, routing):
     T, E, k, H, I = cfg.T, cfg.E, cfg.k, cfg.H, cfg.I
     st_off, _ = mm.mm_workspace_region("stage", T, E, k, H, I)
     l1_off, _ = mm.mm_workspace_region("l1_acts", T, E, k, H, I)
-    sf_off, _ = mm.mm_workspace_region("l1_acts_sf", T, E, k, H, I)
     stage = ws[st_off:st_off + T * k * H * 4].view(torch.float32).view(T * k, H)
     l1a = ws[l1_off:l1_off + T * k * I].view(T * k, I)
-    l1s = ws[sf_off:sf_off + T * k * (I // 32)].view(T * k, I // 32)
+    l1s = token_scale_rows(ws, cfg, "l1_acts_sf", mm.mm_layer_variant(T, E, k, H), idx=tok.idx_np)
     cache = ExpertCache(cfg)
     w_flat = tok.w_np.reshape(-1).astype(np.float64)
     report = {}
@@ -128,7 +127,7 @@ def _dense_expert_parity(cfg, ws, tok, routing):
         fl = torch.from_numpy(flats.astype(np.int64)).cuda()
         got = stage.index_select(0, fl).cpu().numpy().astype(np.float64)
         # 1. L1 activations
-        g = OF.dequantize(l1a.index_select(0, sl).cpu().numpy(), l1s.index_select(0, sl).cpu().numpy(), OF.E4M3)
+        g = OF.dequantize(l1a.index_select(0, sl).cpu().numpy(), l1s[slots], OF.E4M3)
         r = OF.dequantize(codes, sf, OF.E4M3)
         step = np.ldexp(1.0, np.frexp(np.maximum(np.abs(r), np.abs(g)))[1] - 4)   # one E4M3 step
         assert np.all(np.abs(g - r) <= step + 1e-300), (cfg.name, e)
