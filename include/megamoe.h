@@ -386,13 +386,13 @@ int mm_f8b_forward(int num_tokens, int experts, int topk, int hidden, int inter,
  * accounting), plugins that run inside such a host and are handed only their
  * inputs and outputs, and real-time or safety-certified loops that forbid any
  * allocation after start-up.  For them the library keeps one fixed scratch
- * array of 48 MiB in device memory (a file-scope __device__ array, present on
+ * array of 64 MiB in device memory (a file-scope __device__ array, present on
  * every GPU where the library's kernels are loaded until the process exits),
  * enough for a decode batch of the DeepSeek-sized layer (128 tokens, top-8,
- * hidden 7168, inter 2048 needs 39 MB).
+ * 256 experts, hidden 7168, inter 2048 needs 56.2 MiB).
  *
  * Arguments are those of mm_forward minus the workspace.  A shape whose
- * workspace (mm_workspace_size) exceeds 48 MiB is rejected with
+ * workspace (mm_workspace_size) exceeds 64 MiB is rejected with
  * MM_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.  No cudaMalloc,
  * cudaFree or allocating routine is called.  The first call on a device looks
  * up the array's device address (cudaGetSymbolAddress, with that device

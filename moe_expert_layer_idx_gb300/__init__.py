@@ -259,7 +259,7 @@ def prepare_weight_scales(sf, k, stream=None):
 
 def mm_forward_noalloc(num_tokens, experts, topk, hidden, inter, x, x_sf, topk_idx, topk_w, l1_w, l1_sf,
                        l2_w, l2_sf, y, clamp, num_sms, stream=None) -> int:
-    """mm_forward with the library's fixed 48 MiB device scratch as workspace,
+    """mm_forward with the library's fixed 64 MiB device scratch as workspace,
     for callers that cannot allocate device memory (see include/megamoe.h);
     device-side errors are read with mm_noalloc_get_status."""
     return lib().mm_forward_noalloc(num_tokens, experts, topk, hidden, inter, _ptr(x), _ptr(x_sf),

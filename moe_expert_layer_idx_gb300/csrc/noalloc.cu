@@ -15,7 +15,7 @@
 
 namespace {
 
-constexpr size_t kNoAllocScratchBytes = 48ull << 20;   // 48 MiB
+constexpr size_t kNoAllocScratchBytes = 64ull << 20;   // 64 MiB
 
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 

@@ -1,7 +1,7 @@
 """mm_forward_noalloc: the layer for callers that cannot allocate device
 memory where they run it (a runtime whose pool allocator owns all device
 memory, a plugin handed only its inputs and outputs, a loop that forbids
-allocation after start-up).  Its workspace is the library's fixed 48 MiB
+allocation after start-up).  Its workspace is the library's fixed 64 MiB
 device array, and mm_noalloc_get_status reads that array's status word.
 
 Checked through the C ABI against mm_forward with a caller-owned workspace,
@@ -90,7 +90,7 @@ def test_noalloc_reports_a_bad_index_then_recovers():
 def test_noalloc_refuses_shapes_beyond_its_scratch():
     # 1024 tokens x top-8 at hidden 7168 needs ~300 MB of workspace
     big = synth.Config("too-big", T=1024, H=7168, I=2048, E=256, k=8, clamp=7.0)
-    assert mm.mm_workspace_size(big.T, big.E, big.k, big.H, big.I) > 48 << 20
+    assert mm.mm_workspace_size(big.T, big.E, big.k, big.H, big.I) > 64 << 20
     x = torch.empty(16, dtype=torch.uint8, device="cuda")
     rc = mm.mm_forward_noalloc(big.T, big.E, big.k, big.H, big.I, x, x, x, x, x, x, x, x, x, 7.0, 0)
     assert rc == mm.MM_ERR_WORKSPACE_TOO_SMALL
