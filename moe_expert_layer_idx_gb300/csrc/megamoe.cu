@@ -7,19 +7,21 @@
 // progress when every CTA is resident at once; the reserve keeps that true
 // while another stream holds a few SMs.  Phases:
 //
-//  0. dispatch: every warp copies expert-sorted token rows (and their UE8M0
-//     scales) into the workspace and bumps that expert's arrival counter with
-//     a release.  The pages' dispatch pulls each token's row and scales from
+//  0. dispatch: every warp copies expert-sorted token rows into the workspace,
+//     writes their UE8M0 scales into the token block's scale atoms, and bumps
+//     that expert's arrival counter with a release.  The pages' dispatch pulls each token's row and scales from
 //     whichever rank holds it and then releases a per-expert arrival count
 //     (DeepGEMM SM90 MegaMoE dev log, Phase 2 entry); here every row is local.
 //  1. tiles, warp-specialised, dynamically scheduled (see TileFeed):
-//       warps 0 and 3, lane 0  TMA producers; they split each stage's boxes;
+//       warps 0 and 3, lane 0  TMA producers; they split each stage's boxes
+//                              (in the thin tiles also its scale atoms, by bulk
+//                              copies onto the same barrier);
 //       warp 1, lane 0         MMA issuer: scale atoms -> TMEM (tcgen05.cp),
 //                              then 4 x tcgen05.mma kind::mxf8f6f4 block_scale
 //                              (K = 32 each) per 128-wide K stage;
-//       warp 2                 scale loader: loads the UE8M0 bytes of four
-//                              stages into registers, then writes each stage's
-//                              32x4x4 scale atoms with shared-memory stores;
+//       warp 2                 scale loader of the 128-token tiles: copies each
+//                              stage's ready-made scale atoms (token rows, both
+//                              weight halves) with coalesced 16-byte loads;
 //       warps 4-11             epilogue: warp w reads TMEM lanes 32(w%4)..+31,
 //                              the two warps of a lane quarter split the columns.
 //     The MMA puts up to 128 tokens of one expert on M (E4M3, operand A) and

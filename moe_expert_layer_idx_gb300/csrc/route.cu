@@ -1,5 +1,6 @@
 // Routing: per-launch reset, expert histogram, prefix scan, stable
-// permutation and the per-expert N-block table of the persistent kernel.
+// permutation, and the token-block tables of the persistent kernel (each
+// expert's first block, and one record per block).
 //
 // The pages' kernel does this as the first part of its dispatch: it clears
 // its workspace, counts the assignments of each expert and records, for every
