@@ -782,6 +782,10 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
         const size_t wr0 = ti.layer == 1 ? ((size_t)ti.e * (2 * p.I / 128) + ti.nb) * kb
                                          : ((size_t)ti.e * (p.H / 128) + (ti.nb * kTileN + hh * nh) / 128) * kb;
         const size_t wr1 = ti.layer == 1 ? wr0 + (size_t)(p.I / 128) * kb : wr0;
+        // The three scales of stage kk + 1 are loaded while stage kk's partial is added.  The token
+        // scales are read only after the first partial has landed: its MMAs waited (through the
+        // producers) for the token rows, and so for their scales, to be complete.
+        float sx_n = 0.f, w0_n = 0.f, w1_n = 0.f;
         for (int kk = 0; kk < kb; ++kk) {
           const uint32_t pb = pc & 1u, pph = (pc >> 1) & 1u;
           ++pc;
@@ -790,22 +794,37 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
           got = __shfl_sync(0xffffffffu, got, 0);
           if (got) {
             tc_fence_after();
+            if (kk == 0) {
+              sx_n = valid ? __ldcg(tok_s) : 0.f;
+              w0_n = __ldg(w_s + wr0);
+              w1_n = __ldg(w_s + wr1);
+            }
+            const float sx = sx_n, w0 = w0_n, w1 = w1_n;
+            if (kk + 1 < kb) {
+              sx_n = valid ? __ldcg(tok_s + kk + 1) : 0.f;
+              w0_n = __ldg(w_s + wr0 + kk + 1);
+              w1_n = __ldg(w_s + wr1 + kk + 1);
+            }
             if (live_warp) {
-              const float sx = valid ? __ldcg(tok_s + kk) : 0.f;
-              const float c0 = sx * __ldg(w_s + wr0 + kk), c1 = sx * __ldg(w_s + wr1 + kk);
+              const float c0 = sx * w0, c1 = sx * w1;
               const uint32_t pbase = tbase + 256u * pb;
+              // four 16-column loads per TMEM round trip (64 contiguous columns: one operand's
+              // half in L1, this warp's first or second 64 outputs in L2)
 #pragma unroll
-              for (int j = 0; j < 8; ++j) {
+              for (int j = 0; j < 8; j += 4) {
                 const bool l1 = ti.layer == 1;
                 if (!l1 && j * 16 >= nh) break;
-                const uint32_t col = l1 ? (uint32_t)((j < 4 ? 0 : kL1Feat) + hh * 64 + (j & 3) * 16)
-                                        : (uint32_t)(hh * nh + j * 16);
-                float t16[16];
-                tc_ld16(pbase + col, t16);
+                const uint32_t col0 = l1 ? (uint32_t)((j < 4 ? 0 : kL1Feat) + hh * 64)
+                                         : (uint32_t)(hh * nh + j * 16);
+                float t[4][16];
+#pragma unroll
+                for (int x = 0; x < 4; ++x) tc_ld16(pbase + col0 + 16 * x, t[x]);
                 tc_wait_ld();
                 const float c = (l1 && j >= 4) ? c1 : c0;
 #pragma unroll
-                for (int i = 0; i < 16; ++i) v[j * 16 + i] = fmaf(t16[i], c, v[j * 16 + i]);
+                for (int x = 0; x < 4; ++x)
+#pragma unroll
+                  for (int i = 0; i < 16; ++i) v[(j + x) * 16 + i] = fmaf(t[x][i], c, v[(j + x) * 16 + i]);
               }
             }
           } else {
