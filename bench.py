@@ -369,16 +369,17 @@ def run_ours(args, rank, world, local_rank):
     stream = torch.cuda.current_stream(dev)
     torch.cuda.synchronize(dev)
 
-    def step():
+    def forward_into(x_, x_sf_, idx_, w_, y_):
         if bf16_layer:
-            rc = mm.mm_bf16_forward(T, E, k, H, I, x, topk_idx, topk_w, l1_w, l2_w, y, cfg.clamp, 0, ws, ws_bytes,
-                                    stream)
-        elif f8b:
-            rc = mm.mm_f8b_forward(T, E, k, H, I, x, x_sf, topk_idx, topk_w, l1_w, l1_sf, l2_w, l2_sf, y, cfg.clamp,
-                                   0, ws, ws_bytes, stream)
-        else:
-            rc = mm.mm_forward(T, E, k, H, I, x, x_sf, topk_idx, topk_w, l1_w, l1_sf, l2_w, l2_sf, y, cfg.clamp, 0,
-                               ws, ws_bytes, stream)
+            return mm.mm_bf16_forward(T, E, k, H, I, x_, idx_, w_, l1_w, l2_w, y_, cfg.clamp, 0, ws, ws_bytes, stream)
+        if f8b:
+            return mm.mm_f8b_forward(T, E, k, H, I, x_, x_sf_, idx_, w_, l1_w, l1_sf, l2_w, l2_sf, y_, cfg.clamp,
+                                     0, ws, ws_bytes, stream)
+        return mm.mm_forward(T, E, k, H, I, x_, x_sf_, idx_, w_, l1_w, l1_sf, l2_w, l2_sf, y_, cfg.clamp, 0,
+                             ws, ws_bytes, stream)
+
+    def step():
+        rc = forward_into(x, x_sf, topk_idx, topk_w, y)
         if rc != mm.MM_OK:
             raise RuntimeError(f"mm_forward: {mm.STATUS_NAMES.get(rc, rc)}")
 
@@ -449,32 +450,91 @@ def run_ours(args, rank, world, local_rank):
     hsf = x_sf.cpu().pin_memory() if x_sf is not None else None
     hidx = topk_idx.cpu().pin_memory()
     hw = topk_w.cpu().pin_memory()
-    hy = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
     e_steps = max(1, min(args.steps, 200))
-
-    def e2e_step():
-        x.copy_(hx, non_blocking=True)
-        if hsf is not None:
-            x_sf.copy_(hsf, non_blocking=True)
-        topk_idx.copy_(hidx, non_blocking=True)
-        topk_w.copy_(hw, non_blocking=True)
-        step()
-        hy.copy_(y, non_blocking=True)
-
-    for _ in range(2):
-        e2e_step()
-    barrier()
-    e0_, e1_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0_.record(stream)
-    for _ in range(e_steps):
-        e2e_step()
-    e1_.record(stream)
-    e1_.synchronize()
-    check_status()
-    e2e_tps, e2e_ms = replica_throughput(e0_.elapsed_time(e1_) / e_steps, T, world, max_over_ranks)
     h2d = hx.numel() * hx.element_size() + (hsf.numel() * hsf.element_size() if hsf is not None else 0) + \
         hidx.numel() * 4 + hw.numel() * 4
-    d2h = hy.numel() * 2
+    d2h = T * H * 2
+
+    def e2e_serial():
+        """Every step on one stream: upload, layer, download, one after the other."""
+        hy = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
+
+        def one():
+            x.copy_(hx, non_blocking=True)
+            if hsf is not None:
+                x_sf.copy_(hsf, non_blocking=True)
+            topk_idx.copy_(hidx, non_blocking=True)
+            topk_w.copy_(hw, non_blocking=True)
+            step()
+            hy.copy_(y, non_blocking=True)
+
+        for _ in range(2):
+            one()
+        barrier()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(e_steps):
+            one()
+        b.record(stream)
+        b.synchronize()
+        return a.elapsed_time(b) / e_steps
+
+    def e2e_pipelined():
+        """Two sets of device buffers; step i + 1's upload (one copy stream) and step
+        i - 1's download (another) overlap step i's layer.  The timed region still
+        holds every step's upload, layer and download: it starts before the first
+        upload and ends after the last download."""
+        up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        bufs = []
+        for _b in range(2):
+            bufs.append({"x": torch.empty_like(x), "x_sf": torch.empty_like(x_sf) if x_sf is not None else None,
+                         "idx": torch.empty_like(topk_idx), "w": torch.empty_like(topk_w), "y": torch.empty_like(y),
+                         "hy": torch.empty(T, H, dtype=torch.bfloat16).pin_memory(),
+                         "in": torch.cuda.Event(), "out": torch.cuda.Event(), "d2h": torch.cuda.Event()})
+        for bf in bufs:
+            bf["out"].record(stream)
+            bf["d2h"].record(stream)
+
+        def run(n):
+            for i in range(n):
+                bf = bufs[i % 2]
+                up.wait_event(bf["out"])                  # the layer two steps back has read these inputs
+                with torch.cuda.stream(up):
+                    bf["x"].copy_(hx, non_blocking=True)
+                    if hsf is not None:
+                        bf["x_sf"].copy_(hsf, non_blocking=True)
+                    bf["idx"].copy_(hidx, non_blocking=True)
+                    bf["w"].copy_(hw, non_blocking=True)
+                bf["in"].record(up)
+                stream.wait_event(bf["in"])
+                stream.wait_event(bf["d2h"])              # the download two steps back has read y
+                rc = forward_into(bf["x"], bf["x_sf"], bf["idx"], bf["w"], bf["y"])
+                if rc != mm.MM_OK:
+                    raise RuntimeError(f"forward failed: {mm.STATUS_NAMES.get(rc, rc)}")
+                bf["out"].record(stream)
+                down.wait_event(bf["out"])
+                with torch.cuda.stream(down):
+                    bf["hy"].copy_(bf["y"], non_blocking=True)
+                bf["d2h"].record(down)
+            for bf in bufs:                                # the last downloads end the timed region
+                stream.wait_event(bf["d2h"])
+
+        run(2)
+        barrier()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        up.wait_event(a)
+        run(e_steps)
+        b.record(stream)
+        b.synchronize()
+        return a.elapsed_time(b) / e_steps
+
+    serial_ms = e2e_serial()
+    check_status()
+    pipe_ms = e2e_pipelined()
+    check_status()
+    e2e_tps, e2e_ms = replica_throughput(pipe_ms, T, world, max_over_ranks)
+    serial_tps, serial_ms = replica_throughput(serial_ms, T, world, max_over_ranks)
 
     roofline = _roofline(cfg, ms, idx_np, bf16_layer, args.workload,
                          "whole step: routing + megamoe_kernel + combine_kernel", route_ms, f8b)
@@ -512,7 +572,10 @@ def run_ours(args, rank, world, local_rank):
     return {
         "tokens_per_s": tokens_per_s, "ms": ms, "route_ms": route_ms, "roofline": roofline,
         "e2e": {"value": round(e2e_tps, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
+                "copies": "two copy streams: step i+1's upload and step i-1's download overlap step i's layer",
+                "serial": {"value": round(serial_tps, 1), "ms_per_step": round(serial_ms, 4),
+                           "copies": "upload, layer, download in order on one stream"}},
         "clocks": clk.summary(), "wall_s": t_wall, "gpu_launches": launches_per_step * args.steps, "step_ms": pct,
         "cfg": cfg, "per_config": per_config,
     }

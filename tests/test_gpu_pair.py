@@ -136,3 +136,30 @@ def test_pair_bad_index_then_recovers():
     xc, xsf = oracle_tokens(cfg)
     ref = OM.moe_forward(xc, xsf, routing[0], routing[1], ExpertCache(cfg), cfg.clamp, cfg.E)
     assert close_enough(bf16_to_np(y2), ref)[0]
+
+
+def test_pair_bf16_activations_equal_quantize_then_forward():
+    """mm_forward_bf16 with two-CTA tiles: the dispatch quantises each token
+    and writes its scales into both 128-row halves of the token blocks' scale
+    atoms; the result equals mm_forward on mm_quantize_mx of the same values,
+    bit for bit (blocks of 150 rows: 128 on the even CTA, 22 on the odd one)."""
+    from layer_inputs import gpu_quantize
+    cfg = CASES["pair-two-blocks"]
+    T, H = cfg.T, cfg.H
+    assert mm.mm_layer_variant(T, cfg.E, cfg.k, H) == PAIR
+    w = GpuWeights(cfg)
+    tok = GpuTokens(cfg)
+    xf = torch.empty(T * H, dtype=torch.float32, device="cuda")
+    synth.normal_f32_cuda(cfg.seed, synth.TENSOR_X, 0, xf)
+    xb = xf.view(T, H).to(torch.bfloat16)
+    ws = torch.empty(mm.mm_workspace_size(T, cfg.E, cfg.k, H, cfg.I), dtype=torch.uint8, device="cuda")
+    y_fold = torch.empty(T, H, dtype=torch.bfloat16, device="cuda")
+    assert mm.mm_forward_bf16(T, cfg.E, cfg.k, H, cfg.I, xb, tok.topk_idx, tok.topk_w, w.l1_w, w.l1_sf, w.l2_w,
+                              w.l2_sf, y_fold, cfg.clamp, 0, ws) == mm.MM_OK
+    assert mm.mm_get_status(ws)[0] == mm.MM_OK
+    x8, sf8 = gpu_quantize(xb.float().reshape(-1), T, H, mm.MM_FMT_E4M3)
+    y_sep = torch.empty(T, H, dtype=torch.bfloat16, device="cuda")
+    assert mm.mm_forward(T, cfg.E, cfg.k, H, cfg.I, x8, sf8, tok.topk_idx, tok.topk_w, w.l1_w, w.l1_sf, w.l2_w,
+                         w.l2_sf, y_sep, cfg.clamp, 0, ws) == mm.MM_OK
+    assert mm.mm_get_status(ws)[0] == mm.MM_OK
+    assert torch.equal(y_fold.view(torch.int16), y_sep.view(torch.int16))
