@@ -1064,10 +1064,12 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
   }
 }
 
-// The top-k weighted combine, one warp per (token, up to 1024 outputs): 128
-// uint4 chunks of 8 bf16, 4 per lane.  y[t, c] = bf16_RNE(sum over the token's
+// The top-k weighted combine, one warp per (token, 256 outputs): 32 uint4
+// chunks of 8 bf16, one per lane, whose k rows' loads all go out together (a
+// small batch is one round trip per warp, not four).  y[t, c] = bf16_RNE(sum over the token's
 // valid slots j, ascending, of stage[t*k + j, c]), summed in fp32 from zero; a
 // token routed nowhere gets a zero row.  Nothing is combined after an error.
+constexpr int kCombineChunks = 32;   // 8-element chunks per warp item
 __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ ForwardParams p) {
   const uint32_t* ctrl = reinterpret_cast<const uint32_t*>(p.ws + p.L.ctrl);
   if (ld_volatile(&ctrl[kStatus]) != 0u) return;
@@ -1075,7 +1077,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ Fo
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int H = p.H, k = p.k;
   const int nchunk = H / 8;
-  const int per_item = 128;
+  const int per_item = kCombineChunks;
   const int items_per_token = (nchunk + per_item - 1) / per_item;
   const int nitems = p.T * items_per_token;
   const int wpb = blockDim.x >> 5;
@@ -1205,7 +1207,7 @@ cudaError_t layer_launch(int variant, int grid, cudaStream_t stream, const CUten
     default: e = launch_one<WideVariant>(grid, stream, maps, p); break;
   }
   if (e != cudaSuccess) return e;
-  const long long items = (long long)p.T * ((p.H / 8 + 127) / 128);
+  const long long items = (long long)p.T * ((p.H / 8 + kCombineChunks - 1) / kCombineChunks);
   const long long want = (items + 7) / 8;
   const int blocks = (int)std::max(1ll, std::min(want, 8ll * grid));
   combine_kernel<<<blocks, 256, 0, stream>>>(p);
