@@ -545,7 +545,7 @@ def run_ours(args, rank, world, local_rank):
     # ---- the other full-size configurations, timed the same way (1 GPU only)
     per_config = {}
     if world == 1 and args.layer == "fp8" and args.per_config:
-        del hx, hsf, hidx, hw, hy, ws
+        del hx, hsf, hidx, hw, ws
         weights = (l1_w, l1_sf, l2_w, l2_sf)
         for name in args.per_config:
             pc = synth.CONFIGS[name]
