@@ -74,13 +74,17 @@ struct Tile {
 // Tiles are numbered L1 first, then L2; within a layer expert-major, then the
 // weight block, then the token block, so the token blocks that share a weight
 // tile run close together and find it in L2.
-__device__ __forceinline__ void decode_tile(int t, int nL1, const ForwardParams& p, Tile& ti) {
+// An expert's tiles are [items[e] * NB, items[e + 1] * NB), so tt / NB is one
+// of its token blocks, whose record names the expert and its tables.
+__device__ __forceinline__ int4 tile_record(int t, int nL1, const ForwardParams& p) {
+  const bool l1 = t < nL1;
+  const int tt = l1 ? t : t - nL1;
+  return __ldg(reinterpret_cast<const int4*>(p.ws + p.L.blocks) + tt / (l1 ? p.mt1 : p.mt2));
+}
+__device__ __forceinline__ void decode_tile(int t, int nL1, const ForwardParams& p, const int4 rec, Tile& ti) {
   const bool l1 = t < nL1;
   const int tt = l1 ? t : t - nL1;
   const int NB = l1 ? p.mt1 : p.mt2;
-  // An expert's tiles are [items[e] * NB, items[e + 1] * NB), so tt / NB is
-  // one of its token blocks, whose record names the expert and its tables.
-  const int4 rec = __ldg(reinterpret_cast<const int4*>(p.ws + p.L.blocks) + tt / NB);
   const int e = rec.x, i0 = rec.y, cnt = rec.w;
   const int mbk = n_blocks(cnt, p.max_rows);    // token blocks of this expert
   const int local = tt - i0 * NB;
@@ -141,6 +145,8 @@ struct TileFeed {
   uint64_t* empty;
   uint32_t i = 0;
   int ahead = -1;              // producer 0: index claimed for the next publication
+  int4 ahead_rec;              // and its token-block record, once loaded ahead (rec_ready)
+  bool rec_ready = false;
   bool peer = false;           // a reader of the odd CTA of a pair
   uint32_t empty_cl = 0;       // odd CTA: cluster address of the even CTA's empty[0]
   uint32_t peer_ring_cl = 0;   // even CTA's producer 0: the odd CTA's ring[0] and full[0]
@@ -172,8 +178,9 @@ struct TileFeed {
     ++i;
     if (!mbar_wait<true>(smem_u32(&empty[slot]), ph ^ 1u, ctrl, to, kSiteTileRing << 24)) { ok = false; return false; }
     const int t = ahead >= 0 ? ahead : (int)atomicAdd(counter, 1u);
-    if (t < total) decode_tile(t, nL1, p, ti);
+    if (t < total) decode_tile(t, nL1, p, rec_ready ? ahead_rec : tile_record(t, nL1, p), ti);
     else ti.layer = 0;
+    rec_ready = false;
     ring[slot] = ti;
     if (peer_ring_cl != 0) {
       const uint32_t* w = reinterpret_cast<const uint32_t*>(&ti);
@@ -184,6 +191,15 @@ struct TileFeed {
     mbar_arrive(smem_u32(&full[slot]));          // release: the tile is visible to the readers
     ahead = t < total ? (int)atomicAdd(counter, 1u) : -1;   // consumed at the next claim
     return ti.layer != 0;
+  }
+  // Producer 0, part-way through the current tile's loads (the atomic for the
+  // next index has returned by then): the next tile's record is loaded now, so
+  // the next claim decodes it without a memory round trip.
+  __device__ void prefetch(int total, int nL1, const ForwardParams& p) {
+    if (!rec_ready && ahead >= 0 && ahead < total) {
+      ahead_rec = tile_record(ahead, nL1, p);
+      rec_ready = true;
+    }
   }
   // One reading thread.
   __device__ bool take(uint32_t* ctrl, unsigned long long to, bool& ok, Tile& ti) {
@@ -541,6 +557,7 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
           }
           ++issued;
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
+          if (claimer && kk0 == 2 * kSub) feed.prefetch(total, nL1, p);
         }
       }
       s_misc[2 + 3 * pid] = issued;     // s_misc[2] (producer 0), s_misc[5] (producer 1)
