@@ -83,6 +83,18 @@ def test_routing_in_workspace(case):
     assert np.array_equal(p[:n], inter["perm"]) and np.array_equal(i, inter["inv"])
 
 
+def test_dispatched_scales_are_the_tokens_scales(case):
+    """The dispatch writes each slot's UE8M0 scale bytes into its token
+    block's scale atoms; read back into rows, slot s holds exactly the
+    x_sf row of the token perm[s] // k."""
+    cfg, w, tok, y, ws, ref, inter = case
+    variant = mm.mm_layer_variant(cfg.T, cfg.E, cfg.k, cfg.H)
+    got = token_scale_rows(ws, cfg, "xs_sf", variant, idx=tok.idx_np)
+    xsf = tok.x_sf.cpu().numpy()
+    want = xsf[inter["perm"] // cfg.k]
+    assert np.array_equal(got, want), cfg.name
+
+
 def test_l1_activations_close_to_oracle(case):
     """Diagnostic of the requantised L1 activations: the GPU accumulates in
     fp32 and the oracle in fp64, so a code may move by one step near a
