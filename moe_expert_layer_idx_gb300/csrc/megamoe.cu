@@ -420,22 +420,35 @@ megamoe_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant_
       for (int u = 0; u < kBatch; ++u) fs[u] = s0 + u * G < nvalid ? __ldg(perm + s0 + u * G) : -1;
 #pragma unroll
       for (int u = 0; u < kBatch; ++u) es[u] = fs[u] >= 0 ? __ldg(p.topk_idx + fs[u]) : -1;
+      // the rows go two at a time: both rows' loads (up to 8 per lane each) in flight together
+#pragma unroll
+      for (int u0 = 0; u0 < kBatch; u0 += 2) {
+        const bool h0 = fs[u0] >= 0, h1 = fs[u0 + 1] >= 0;   // warp-uniform
+        const uint4* src0 = reinterpret_cast<const uint4*>(p.x + (size_t)(h0 ? fs[u0] / p.k : 0) * H * esz);
+        const uint4* src1 = reinterpret_cast<const uint4*>(p.x + (size_t)(h1 ? fs[u0 + 1] / p.k : 0) * H * esz);
+        uint4* dst0 = reinterpret_cast<uint4*>(xs + (size_t)(s0 + u0 * G) * H * esz);
+        uint4* dst1 = reinterpret_cast<uint4*>(xs + (size_t)(s0 + (u0 + 1) * G) * H * esz);
+        for (int c0 = lane; c0 < nvec; c0 += 32 * 8) {
+          uint4 v0[8], v1[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            if (h0 && c0 + 32 * i < nvec) v0[i] = __ldg(src0 + c0 + 32 * i);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            if (h1 && c0 + 32 * i < nvec) v1[i] = __ldg(src1 + c0 + 32 * i);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            if (h0 && c0 + 32 * i < nvec) dst0[c0 + 32 * i] = v0[i];
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            if (h1 && c0 + 32 * i < nvec) dst1[c0 + 32 * i] = v1[i];
+        }
+      }
 #pragma unroll
       for (int u = 0; u < kBatch; ++u) {
         if (fs[u] < 0) continue;                      // warp-uniform
         const int s = s0 + u * G;
         const int t = fs[u] / p.k;
-        const uint4* src = reinterpret_cast<const uint4*>(p.x + (size_t)t * H * esz);
-        uint4* dst = reinterpret_cast<uint4*>(xs + (size_t)s * H * esz);
-        for (int c0 = lane; c0 < nvec; c0 += 32 * 16) {     // 16 independent loads in flight per lane
-          uint4 v[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            if (c0 + 32 * i < nvec) v[i] = __ldg(src + c0 + 32 * i);
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            if (c0 + 32 * i < nvec) dst[c0 + 32 * i] = v[i];
-        }
         if constexpr (V::kF8B) {
           // fp32 scale per 128 elements: rows of H / 32 bytes, in slot order
           const uint32_t* ssf = reinterpret_cast<const uint32_t*>(p.x_sf + (size_t)t * (H / 32));
