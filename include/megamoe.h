@@ -256,7 +256,7 @@ int mm_get_status(const void* workspace, mm_stream_t stream, int* sm, int* info)
 /*
  * mm_route -- runs only the routing of mm_forward (reset, expert histogram,
  * prefix scan, stable permutation) into `workspace` ([P3] Phase 2 entry:
- * expert count, source token-topk index write): one kernel up to 2048
+ * the per-expert counts and each slot's source assignment): one kernel up to 2048
  * assignments, else three (per-chunk counts, scan, scatter).  Same argument
  * rules as mm_forward.  Test hook.
  */

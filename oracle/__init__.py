@@ -13,8 +13,8 @@ What it computes (the single-GPU fused MegaMoE expert layer):
   quantiser (the recipe ``(1, 1, 32)`` of DeepGEMM ``fp8_fp4_mega_moe``,
   quoted on the digest page of sglang PR #36657, section 关键源码片段).
 * ``routing``  -- per-expert counts, exclusive prefix offsets and the stable
-  permutation (the dispatch steps "expert count" and "source token-topk index
-  write" of the DeepGEMM SM90 MegaMoE dev log, Phase 2 entry).
+  permutation (the counting and source-recording steps of the dispatch in
+  the DeepGEMM SM90 MegaMoE dev log, Phase 2 entry).
 * ``moe``      -- the layer: L1 gate/up GEMM, clamp, SwiGLU, FP8 requantisation
   of the L1 activations, L2 down GEMM, and the top-k weighted combine into a
   bf16 output, accumulated in fp64.

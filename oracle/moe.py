@@ -14,10 +14,10 @@ DeepGEMM kernel is not part of it):
    o = h . W2[e]^T                          (L2 down GEMM, fp64 sums)
 4. y[t] = bf16_RNE( sum over j ascending of topk_w[t, j] * o_(t,j) ).
 
-Sources: the fused call ``deep_gemm.fp8_fp4_mega_moe(y, l1_weights,
-l2_weights, buf, recipe=(1, 1, 32), activation="swiglu",
-activation_clamp=swiglu_limit, fast_math=True)`` and the ``y[:num_tokens]``
-slice (digest page of sglang PR #36657, 关键源码片段); the buffer views x,
+Sources: the fused FP8 x FP4 MegaMoE call on the digest page of sglang PR
+#36657 (section 关键源码片段): it takes the output, both layers' weights and
+a shared buffer, the per-32 (1, 1, 32) recipe, SwiGLU with an optional
+activation clamp, and keeps the first num_tokens output rows; the buffer views x,
 x_sf, topk_idx, topk_weights, l1_acts, l1_acts_sf, l2_acts, l2_acts_sf
 (DeepGEMM SM90 MegaMoE dev log, Phase 1 entry); the dispatch/combine
 ordering (same log, Phase 2 entry; DeepGEMM PR #451 "Reset MegaMoE combine

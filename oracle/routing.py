@@ -1,8 +1,8 @@
 """Routing of (token, k) assignments to experts -- plain definitions.
 
-Follows the dispatch steps of the DeepGEMM SM90 MegaMoE dev log (Phase 2
-entry: "expert count", "source token-topk index" write, token source
-metadata) restricted to one GPU:
+Follows the dispatch steps that the DeepGEMM SM90 MegaMoE dev log lists in
+its Phase 2 entry (count each expert's assignments, record for every slot
+which token and top-k position it came from), restricted to one GPU:
 
 * counts[e]   = number of assignments (t, j) with topk_idx[t, j] == e;
 * offsets[e]  = sum of counts[e'] for e' < e  (offsets has E + 1 entries);
