@@ -14,9 +14,8 @@ values.
 
 Workload recipe (the configurations of the fused MegaMoE expert layer on the
 pages "[Blackwell] Reserve SMs for DeepGEMM MegaMoE grid barriers", Summary /
-Fix, and the DeepGEMM `fp8_fp4_mega_moe(..., recipe=(1, 1, 32),
-activation="swiglu", activation_clamp=...)` call quoted on the digest of the
-same PR, "关键源码片段"):
+Fix, and the DeepGEMM FP8 x FP4 MegaMoE call (per-32 recipe, SwiGLU with an
+activation clamp) shown on the digest of the same PR, section 关键源码片段):
 
 * x  ~ N(0, 1)           [T, H]        tensor id 1
 * W1 ~ N(0, 1/sqrt(H))   [E, 2I, H]    tensor id 2   (rows [0, I) gate, [I, 2I) up)
