@@ -236,8 +236,8 @@ int mm_grid_size(int device_sms, int reserved_sms, int num_sms, int max_resident
 
 /*
  * mm_set_wait_timeout_ns -- time limit of every device-side wait (default
- * 2e9 ns).  The pages' kernel reports "grid sync timeout: sm=.., thread=..,
- * grid_sync_idx=.." instead of hanging ([P2] 功能与动机); here the wait
+ * 2e9 ns).  The pages' kernel reports a grid-sync timeout with the SM, the
+ * thread and the barrier's index instead of hanging ([P2] 功能与动机); here the wait
  * records MM_ERR_TIMEOUT with the SM and the wait site, raises the abort flag
  * and returns.  ns == 0 restores the default.  Process-wide.
  */

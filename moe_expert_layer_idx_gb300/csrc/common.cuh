@@ -163,7 +163,7 @@ enum CtrlWord : int {
 // the numbers are part of the reported value, so a retired site keeps its gap.
 enum WaitSite : uint32_t {
   kSiteFull = 1, kSiteEmpty = 2, kSiteTmemFull = 3, kSiteTmemEmpty = 4,
-  kSiteArrival = 5, kSiteL1Done = 6, kSiteDrain = 8, kSiteFullSf = 9, kSiteTileRing = 10
+  kSiteArrival = 5, kSiteL1Done = 6, kSiteDrain = 8, kSiteTileRing = 10   // 7 and 9: retired
 };
 
 // ----------------------------------------------------------------- workspace

@@ -49,8 +49,9 @@
 // Every wait is bounded (global timer + abort flag): a wait that runs out
 // records MM_ERR_TIMEOUT with the SM and the wait site, raises the abort flag,
 // and the CTA drains its own in-flight copies and MMAs, frees its TMEM and
-// returns -- the pages' kernel reports "grid sync timeout: sm=.., thread=..,
-// grid_sync_idx=.." (digest of PR #36657, 功能与动机) instead of hanging.
+// returns -- the pages' kernel likewise reports a grid-sync timeout with the
+// SM, the thread and the barrier's index (digest of PR #36657, 功能与动机)
+// instead of hanging.
 // All counters are reset by the routing kernel of the same launch, never
 // keyed on %gridid (DeepGEMM PR #451).
 #include "common.cuh"
